@@ -1,0 +1,195 @@
+"""GB300 (sm_103a) fused attention forward: Python binding of the C ABI.
+
+The binding only marshals arguments: every step of the computation runs in the
+CUDA kernels of ``libfa_fwd.so`` (built in-tree by ``build()``), called through
+the C ABI declared in ``include/fa_fwd.h``.  PyTorch provides device memory and
+the current stream.  There is no fallback: if the library is missing, or a call
+returns an error status, the call raises.
+
+    >>> o, lse = fa_fwd(q, k, v, causal=True)      # q, k, v: CUDA [B, H, S, D]
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+from . import _build
+
+__all__ = ["fa_fwd", "fa_fwd_hostio", "launch_info", "plan", "device_status",
+           "selftest_wait_timeout", "strerror", "build", "lib", "header_functions",
+           "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
+           "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FaError"]
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
+_DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+HEADER = os.path.join(_build.ROOT, "include", "fa_fwd.h")
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {strerror(status)} (status {status})")
+        self.status = status
+
+
+class LaunchInfo(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int), ("block", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("tiles_per_unit", ctypes.c_int), ("units", ctypes.c_int),
+                ("head_group", ctypes.c_int), ("num_sms", ctypes.c_int)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library for sm_103a (nvcc) if it is missing or stale."""
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"{_build.LIB} is missing: build it with attention_fa_fwd_gb300.build()")
+        L = ctypes.CDLL(_build.LIB)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        dims = [i, i, i, i, i, f, i, vp]
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp] + dims
+        L.fa_fwd_hostio.argtypes = [vp] * 10 + dims
+        L.fa_fwd_launch_info.argtypes = [i, i, i, i, i, i, ctypes.POINTER(LaunchInfo)]
+        L.fa_fwd_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(LaunchInfo)]
+        L.fa_device_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint)]
+        L.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        L.fa_strerror.argtypes = [i]
+        L.fa_strerror.restype = ctypes.c_char_p
+        for name in ("fa_fwd", "fa_fwd_hostio", "fa_fwd_launch_info", "fa_fwd_plan",
+                     "fa_device_status", "fa_selftest_wait_timeout"):
+            getattr(L, name).restype = i
+        _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/fa_fwd.h declares."""
+    with open(HEADER, encoding="utf-8") as fh:
+        text = fh.read()
+    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
+
+
+def strerror(status: int) -> str:
+    return lib().fa_strerror(int(status)).decode()
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, S, D]")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k, v must share one [B, H, S, D] shape")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPE:
+        raise ValueError("q, k, v must all be float16 or all bfloat16")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+
+
+def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+           scale: float | None = None, out: torch.Tensor | None = None,
+           lse: torch.Tensor | None = None, stream=None):
+    """O, LSE of softmax(Q K^T * scale + causal mask) V on the current CUDA stream.
+
+    q, k, v: contiguous CUDA [B, H, S, D] float16/bfloat16 (D in {64, 128}).
+    Returns (o [B, H, S, D] in the input dtype, lse [B, H, S] float32, natural log).
+    """
+    _check_qkv(q, k, v)
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != q.device:
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse.shape != (B, H, S) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous float32 [B, H, S] tensor on q's device")
+    with torch.cuda.device(q.device):
+        rc = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                          B, H, S, D, int(bool(causal)), float(scale), _DTYPE[q.dtype],
+                          _stream_ptr(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return out, lse
+
+
+def fa_fwd_hostio(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, causal: bool = False,
+                  scale: float | None = None, stream=None):
+    """Host-buffer form: copies q/k/v in, runs the pass, copies o/lse out, all
+    enqueued on the stream (the caller synchronises).  Host tensors should be
+    pinned; device tensors are the caller's [B, H, S, D] / [B, H, S] buffers."""
+    B, H, S, D = q_h.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dt = q_h.dtype
+    if dt not in _DTYPE:
+        raise ValueError("dtype must be float16 or bfloat16")
+    for t in (q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d):
+        if not t.is_contiguous():
+            raise ValueError("every buffer must be contiguous")
+    with torch.cuda.device(q_d.device):
+        rc = lib().fa_fwd_hostio(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(),
+                                 lse_h.data_ptr(), q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(),
+                                 o_d.data_ptr(), lse_d.data_ptr(), B, H, S, D, int(bool(causal)),
+                                 float(scale), _DTYPE[dt], _stream_ptr(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_hostio")
+
+
+def launch_info(B: int, H: int, S: int, D: int, causal: bool, dtype=torch.bfloat16) -> dict:
+    """Launch geometry on the current device (host query, launches nothing)."""
+    info = LaunchInfo()
+    rc = lib().fa_fwd_launch_info(B, H, S, D, int(bool(causal)), _DTYPE.get(dtype, 99),
+                                  ctypes.byref(info))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_launch_info")
+    return info.as_dict()
+
+
+def plan(B: int, H: int, S: int, D: int, causal: bool, num_sms: int, dtype=torch.bfloat16) -> dict:
+    """Launch geometry for a device with `num_sms` SMs (pure host computation)."""
+    info = LaunchInfo()
+    rc = lib().fa_fwd_plan(B, H, S, D, int(bool(causal)), _DTYPE.get(dtype, 99), num_sms,
+                           ctypes.byref(info))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_plan")
+    return info.as_dict()
+
+
+def device_status(clear: bool = True, stream=None) -> tuple[int, int]:
+    """(status, site) of the bounded in-kernel waits; synchronises the stream."""
+    site = ctypes.c_uint(0)
+    rc = lib().fa_device_status(_stream_ptr(stream), int(bool(clear)), ctypes.byref(site))
+    if rc not in (FA_OK, FA_ERR_TIMEOUT):
+        raise FaError(rc, "fa_device_status")
+    return rc, site.value
+
+
+def selftest_wait_timeout(timeout_us: int, stream=None) -> None:
+    rc = lib().fa_selftest_wait_timeout(int(timeout_us), _stream_ptr(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_selftest_wait_timeout")

@@ -1,0 +1,278 @@
+// Host side of the C ABI declared in include/fa_fwd.h: argument checks, TMA
+// tensor maps, launch geometry and the work-unit schedule, dispatch to the
+// kernel instances.  Nothing here allocates device memory.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "fa_fwd.h"
+#include "fa_fwd_common.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+using fa::kBM;
+
+// Device status word: a bounded wait that gives up stores its site here.
+__device__ unsigned int g_fa_status = 0u;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_num_sms[kMaxDevices];     // 0 = not queried yet
+std::atomic<int> g_cc[kMaxDevices];          // major*10 + minor, 0 = not queried yet
+
+unsigned long long timeout_ns()
+{
+    static const unsigned long long ns = [] {
+        const char* e = std::getenv("FA_WAIT_TIMEOUT_MS");
+        long long ms = e ? std::atoll(e) : 0;
+        if (ms <= 0) ms = 4000;
+        return (unsigned long long)ms * 1000000ull;
+    }();
+    return ns;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// SM count and compute capability of the current device (cached per device).
+int device_props(int* num_sms, int* cc)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    int n = g_num_sms[dev].load(std::memory_order_relaxed);
+    int c = g_cc[dev].load(std::memory_order_relaxed);
+    if (n == 0 || c == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        c = major * 10 + minor;
+        g_num_sms[dev].store(n, std::memory_order_relaxed);
+        g_cc[dev].store(c, std::memory_order_relaxed);
+    }
+    *num_sms = n;
+    *cc = c;
+    return FA_OK;
+}
+
+int check_args(int B, int H, int S, int D, int causal, int dtype)
+{
+    if (B < 1 || H < 1 || S < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    // every tensor stays below 2^31 elements (the header's size limit)
+    const long long rows = (long long)B * H * S;
+    if (rows * (long long)(D > 0 ? D : 1) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Work-unit geometry (see the schedule comment in fa_fwd_kernel.cuh).
+void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t* info, fa::Params* p)
+{
+    const int BH = B * H;
+    const int n_qtiles = (S + kBM - 1) / kBM;
+    // two query tiles per unit (ping-pong softmax) once there is enough work for
+    // two units per SM; otherwise one, so small problems still fill the GPU
+    const int tpu = ((long long)BH * n_qtiles >= 2ll * num_sms) ? 2 : 1;
+    const int n_qgroups = (n_qtiles + tpu - 1) / tpu;
+    const long long units = (long long)BH * n_qgroups;
+    const int grid = (int)(units < num_sms ? units : num_sms);
+    int head_group = 1;
+    if (causal) {
+        // a group holds about two rounds of units, so the snake order pairs each
+        // long unit with a short one
+        head_group = (int)((2ll * grid + n_qgroups / 2) / n_qgroups);
+        if (head_group < 1) head_group = 1;
+        if (head_group > BH) head_group = BH;
+    }
+    if (info) {
+        info->grid = grid;
+        info->block = fa::kThreads;
+        info->smem_bytes = fa::smem_bytes_for(D);
+        info->tiles_per_unit = tpu;
+        info->units = (int)units;
+        info->head_group = head_group;
+        info->num_sms = num_sms;
+    }
+    if (p) {
+        p->BH = BH;
+        p->S = S;
+        p->n_qtiles = n_qtiles;
+        p->n_kv = n_qtiles;
+        p->tpu = tpu;
+        p->n_qgroups = n_qgroups;
+        p->n_units = (int)units;
+        p->head_group = head_group;
+        p->causal = causal;
+        p->mask_last = (causal || (S % fa::kBN) != 0) ? 1 : 0;
+    }
+}
+
+// [B*H, S, D] 16-bit tensor, 128-row x 64-column boxes, 128-byte swizzle.
+int make_tmap(CUtensorMap* m, const void* ptr, int BH, int S, int D, int dtype)
+{
+    auto fn = encode_fn();
+    if (!fn) return FA_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace fa {
+int smem_bytes_for(int D) { return D == 64 ? Cfg<64>::kSmemBytes : Cfg<128>::kSmemBytes; }
+}  // namespace fa
+
+extern "C" {
+
+const char* fa_strerror(int status)
+{
+    switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dim, dtype or device (needs D in {64,128}, fp16/bf16, sm_103)";
+    case FA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA runtime/driver error";
+    case FA_ERR_TIMEOUT: return "a bounded in-kernel wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int fa_fwd_launch_info(int B, int H, int S, int D, int causal, int dtype, fa_launch_info_t* info)
+{
+    if (!info) return FA_ERR_INVALID_ARG;
+    int rc = check_args(B, H, S, D, causal, dtype);
+    if (rc != FA_OK) return rc;
+    int num_sms = 0, cc = 0;
+    rc = device_props(&num_sms, &cc);
+    if (rc != FA_OK) return rc;
+    plan(B, H, S, D, causal, num_sms, info, nullptr);
+    return FA_OK;
+}
+
+int fa_fwd_plan(int B, int H, int S, int D, int causal, int dtype, int num_sms, fa_launch_info_t* info)
+{
+    if (!info || num_sms < 1) return FA_ERR_INVALID_ARG;
+    const int rc = check_args(B, H, S, D, causal, dtype);
+    if (rc != FA_OK) return rc;
+    plan(B, H, S, D, causal, num_sms, info, nullptr);
+    return FA_OK;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D, int causal,
+           float scale, int dtype, void* stream)
+{
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    int rc = check_args(B, H, S, D, causal, dtype);
+    if (rc != FA_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_MISALIGNED;
+    int num_sms = 0, cc = 0;
+    rc = device_props(&num_sms, &cc);
+    if (rc != FA_OK) return rc;
+    if (cc != 103) return FA_ERR_UNSUPPORTED;
+
+    fa::LaunchArgs a;
+    plan(B, H, S, D, causal, num_sms, nullptr, &a.p);
+    fa_launch_info_t info;
+    plan(B, H, S, D, causal, num_sms, &info, nullptr);
+    a.grid = info.grid;
+    a.p.lse = lse;
+    a.p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.p.timeout_ns = timeout_ns();
+    void* status = nullptr;
+    if (cudaGetSymbolAddress(&status, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+    a.p.status = static_cast<unsigned int*>(status);
+    const int BH = B * H;
+    if (make_tmap(&a.tm_q, q, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_k, k, BH, S, D, dtype) != FA_OK ||
+        make_tmap(&a.tm_v, v, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_o, o, BH, S, D, dtype) != FA_OK)
+        return FA_ERR_CUDA;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int e;
+    if (D == 64)
+        e = dtype == FA_DTYPE_BF16 ? fa::launch_d64_bf16(a, s) : fa::launch_d64_f16(a, s);
+    else
+        e = dtype == FA_DTYPE_BF16 ? fa::launch_d128_bf16(a, s) : fa::launch_d128_f16(a, s);
+    return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, void* q_d, void* k_d,
+                  void* v_d, void* o_d, float* lse_d, int B, int H, int S, int D, int causal, float scale, int dtype,
+                  void* stream)
+{
+    if (!q_h || !k_h || !v_h || !o_h || !lse_h || !q_d || !k_d || !v_d || !o_d || !lse_d)
+        return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    int rc = check_args(B, H, S, D, causal, dtype);
+    if (rc != FA_OK) return rc;
+    const void* ptrs[10] = {q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return FA_ERR_MISALIGNED;
+    const size_t n = (size_t)B * H * S * D * 2, nl = (size_t)B * H * S * sizeof(float);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(q_d, q_h, n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(k_d, k_h, n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(v_d, v_h, n, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    rc = fa_fwd(q_d, k_d, v_d, o_d, lse_d, B, H, S, D, causal, scale, dtype, stream);
+    if (rc != FA_OK) return rc;
+    if (cudaMemcpyAsync(o_h, o_d, n, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(lse_h, lse_d, nl, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+int fa_device_status(void* stream, int clear, unsigned int* site)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    unsigned int v = 0u;
+    if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(v)) != cudaSuccess) return FA_ERR_CUDA;
+    if (clear && v != 0u) {
+        const unsigned int zero = 0u;
+        if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    if (site) *site = v;
+    return v == 0u ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream)
+{
+    if (timeout_us < 1u || timeout_us > 10000000u) return FA_ERR_INVALID_ARG;
+    void* status = nullptr;
+    if (cudaGetSymbolAddress(&status, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+    const int e = fa::launch_wait_selftest(static_cast<unsigned int*>(status), (unsigned long long)timeout_us * 1000ull,
+                                           static_cast<cudaStream_t>(stream));
+    return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,595 @@
+// Fused attention forward for sm_103a: a persistent, warp-specialised kernel
+// built on TMA, mbarriers and tcgen05 (tensor memory + single-thread MMA).
+//
+// What is computed, per (batch*head, query row i):
+//   s_ij = scale * q_i . k_j for allowed keys j (all j; or j <= i when causal)
+//   O_i  = sum_j softmax(s_i)_j v_j,   LSE_i = ln sum_j exp(s_ij)
+// ("CUDA手写masked multi-head attention", section 3.1), tile by tile with the
+// running statistics of online softmax and one division at the end
+// ("FlashAttention的Triton性能考古学", 核心算法回顾 and 关键优化：反转循环顺序:
+// the query tile is loaded once and the key loop is inner).
+//
+// CTA layout (512 threads, one CTA per SM, persistent over work units):
+//   warps 0-3   softmax warpgroup of query tile 0 (one thread per row)
+//   warps 4-7   softmax warpgroup of query tile 1
+//   warps 8-11  correction/epilogue warpgroup: O / l, LSE, bf16/fp16 convert,
+//               shared-memory staging and TMA store
+//   warp 12     TMA producer: Q tiles, then a ring of K/V slots
+//   warp 13     tcgen05 MMA issuer (one thread) and TMEM owner
+//   warps 14-15 idle (they complete the fourth warpgroup for setmaxnreg)
+//
+// A work unit is one (batch*head, group of 1 or 2 query tiles of 128 rows).  TMEM
+// (512 columns x 128 lanes, fp32) holds S0 | S1 | O0 | O1: the scores of each
+// query tile, and its output accumulator.  P (16-bit) overwrites the first half
+// of its S region and feeds the P*V MMA straight from TMEM ("G6", V37: P stays
+// in TMEM, the "ts" form of tcgen05.mma).
+//
+// MMA issue order per key tile j ("G6", V39, interleave):
+//   PV0(j), QK0(j+1), PV1(j), QK1(j+1)
+// so the tensor core computes one tile's scores while the other tile's softmax
+// runs.  Because tcgen05.commit covers every earlier MMA of the issuing thread,
+// the commit that announces S_t(j+1) also guarantees PV_t(j) has finished, so
+// the softmax warpgroup may rescale O_t in TMEM right after it sees S_t(j+1).
+//
+// Softmax uses the conditional rescale of "G6", V41, in the base-2 domain: the
+// row base b only moves when the tile maximum exceeds b + 8, so p = 2^(x - b)
+// lies in (0, 256] and O is rescaled (by the warp that owns the rows, only when
+// a row of that warp moved; "G6", V41/V44) in the rare re-base case.
+//
+// Causal masking: with 128 x 128 tiles a query tile's diagonal is exactly its
+// last key tile; later key tiles are skipped, only the diagonal tile (and a
+// ragged last key tile) pays for the mask.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fa_fwd_common.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr float kRebaseThreshold = 8.0f;   // log2 units ("G6", V41: base + 8)
+constexpr float kLn2 = 0.693147180559945309f;
+
+// Register budget per warpgroup after setmaxnreg (sum = 512 for 512 threads at 128).
+constexpr uint32_t kRegSoftmax = 176;
+constexpr uint32_t kRegEpilogue = 64;
+constexpr uint32_t kRegControl = 96;
+
+// Barrier indices inside the barrier array.
+enum : int {
+    kBarQFull = 0,      // [2] Q tile t landed (TMA tx)
+    kBarQEmpty = 2,     // [2] last QK of tile t finished (commit)
+    kBarSFull = 4,      // [2] scores S_t ready (commit)
+    kBarPFull = 6,      // [2] P_t written to TMEM, O_t corrected (4 softmax warps)
+    kBarOFull = 8,      // [2] last PV of tile t finished (commit)
+    kBarOEmpty = 10,    // [2] epilogue done reading O_t (4 epilogue warps)
+    kBarStFull = 12,    // [2] row statistics of tile t in shared memory (4 softmax warps)
+    kBarStEmpty = 14,   // [2] epilogue took the statistics (4 epilogue warps)
+    kBarDrain = 16,     // MMA drain at exit (commit)
+    kBarKVFull = 17,    // [slots] K or V tile landed (TMA tx)
+};
+
+template <int D>
+struct Cfg {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int kTileBytes = kBM * D * 2;          // one Q, K or V tile (16-bit)
+    static constexpr int kBoxBytes = kBM * 64 * 2;          // one 128-row x 64-column swizzle box
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kSlots = (D == 128) ? 4 : 8;        // K/V ring (K and V share it)
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
+    static constexpr int kOffStage = kOffKV + kSlots * kTileBytes;   // one O box for the TMA store
+    static constexpr int kOffStats = kOffStage + kBoxBytes;          // float2 (l, b) [2][128]
+    static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
+    static constexpr int kNumBars = kBarKVEmpty + kSlots;
+    static constexpr int kOffBars = kOffStats + 2 * kBM * 8;
+    static constexpr int kOffCtl = kOffBars + kNumBars * 8;          // [0] TMEM base, [1] abort, [2] epilogue go
+    static constexpr int kSmemBytes = kOffCtl + 16 + 1024;            // + slack to align the base to 1 KB
+    // TMEM columns of the score region S_t and the output accumulator O_t
+    __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
+    __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
+};
+
+struct Unit {
+    int bh;
+    int q_tile[2];   // query tile index of each tile of the unit
+    int nkv[2];      // key tiles to visit per tile (0 = tile absent)
+    int nmax;
+};
+
+// Work units are ordered group of `head_group` heads by group; inside a group
+// the longest units (causal: the last query tiles) come first.  CTA c takes, in
+// round r, entry r*G + c (r even) or r*G + G-1-c (r odd): a snake over a list of
+// falling cost, which evens out the causal triangle, and heads of one group run
+// together so their K/V stay in L2.
+__device__ __forceinline__ int unit_at(int r, const Params& p)
+{
+    const long long G = gridDim.x, c = blockIdx.x;
+    const long long u = (long long)r * G + ((r & 1) ? (G - 1 - c) : c);
+    return u < p.n_units ? (int)u : -1;
+}
+
+__device__ __forceinline__ Unit decode_unit(int u, const Params& p)
+{
+    const int per_group = p.head_group * p.n_qgroups;
+    const int g = u / per_group;
+    const int w = u - g * per_group;
+    const int h0 = g * p.head_group;
+    const int hg = min(p.head_group, p.BH - h0);
+    const int rank = w / hg;
+    Unit un;
+    un.bh = h0 + (w - rank * hg);
+    const int qg = p.causal ? (p.n_qgroups - 1 - rank) : rank;
+    un.nmax = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int qt = qg * p.tpu + t;
+        const bool active = (t < p.tpu) && (qt < p.n_qtiles);
+        un.q_tile[t] = qt;
+        un.nkv[t] = active ? (p.causal ? min(qt + 1, p.n_kv) : p.n_kv) : 0;
+        un.nmax = max(un.nmax, un.nkv[t]);
+    }
+    return un;
+}
+
+// Wait-site codes recorded in the status word: role << 8 | barrier index.
+enum : uint32_t { kSiteSoftmax = 0x100, kSiteEpilogue = 0x300, kSiteLoad = 0x400, kSiteMma = 0x500,
+                  kSiteDrain = 0x600 };
+
+// ---------------------------------------------------------------------------------
+// Softmax warpgroup t: one thread per query row of tile t.
+template <int D, bool kBF16>
+__device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx& wc, int t, uint32_t tmem,
+                                             uint32_t bars, float2* stats)
+{
+    using C = Cfg<D>;
+    const int lane = threadIdx.x & 31;
+    const int wq = (threadIdx.x >> 5) & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::col_s(t);
+    const uint32_t tO = tmem + lane_base + C::col_o(t);
+    const float sl2 = p.scale_log2;
+    uint32_t ph_s = 0, ph_te = 0;
+
+    for (int r = 0;; ++r) {
+        const int u = unit_at(r, p);
+        if (u < 0) break;
+        const Unit un = decode_unit(u, p);
+        const int nkv = un.nkv[t];
+        if (nkv == 0) continue;
+        float b = -INFINITY;   // base of the row, base-2 scaled units
+        float l = 0.f;         // running sum of 2^(x - b)
+        for (int j = 0; j < nkv; ++j) {
+            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + t), ph_s, kSiteSoftmax | (kBarSFull + t))) return;
+            ph_s ^= 1u;
+            ptx::tc_fence_after();
+            uint32_t sr[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sr + 32 * c);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(sr);
+            float* s = reinterpret_cast<float*>(sr);
+            if (p.mask_last && j == nkv - 1) {
+                // keys beyond the sequence, and (causal) keys after this row
+                const int qrow = un.q_tile[t] * kBM + row;
+                int lim = p.S - 1 - j * kBN;
+                if (p.causal) lim = min(lim, qrow - j * kBN);
+#pragma unroll
+                for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+            }
+            float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+#pragma unroll
+            for (int c = 4; c < 128; c += 4) {
+                m0 = fmaxf(m0, s[c]);
+                m1 = fmaxf(m1, s[c + 1]);
+                m2 = fmaxf(m2, s[c + 2]);
+                m3 = fmaxf(m3, s[c + 3]);
+            }
+            const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
+            // conditional re-base: keep b unless the maximum passed b + 8
+            float hist = 1.f;
+            const float cand = fmaxf(b, mx);
+            if (cand > b + kRebaseThreshold) {
+                hist = ptx::ex2(b - cand);   // 0 on the first tile (b = -inf)
+                b = cand;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, hist < 1.f)) {
+                // rare path: scale this warp's 32 rows of O_t (PV_t(j-1) is complete)
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32_wait(tO + c0, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * hist);
+                    ptx::tmem_st32(tO + c0, o);
+                }
+            }
+            const float nb = (b == -INFINITY) ? 0.f : -b;
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ptx::ex2(fmaf(s[c * 32 + 2 * i], sl2, nb));
+                    const float p1 = ptx::ex2(fmaf(s[c * 32 + 2 * i + 1], sl2, nb));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[i] = ptx::pack2<kBF16>(p0, p1);
+                }
+                ptx::tmem_st16(tS + c * 16, pk);
+            }
+            ptx::tmem_wait_st();
+            l = l * hist + (sum0 + sum1);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarPFull + t));
+        }
+        // hand (l, b) of every row to the epilogue
+        if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarStEmpty + t), ph_te ^ 1u, kSiteSoftmax | (kBarStEmpty + t)))
+            return;
+        ph_te ^= 1u;
+        stats[t * kBM + row] = make_float2(l, b);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarStFull + t));
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// Correction/epilogue warpgroup: O_t / l, LSE, convert, stage, TMA store.
+template <int D, bool kBF16>
+__device__ __forceinline__ void epilogue_role(const Params& p, const ptx::WaitCtx& wc, const CUtensorMap* tm_o,
+                                              uint32_t tmem, uint32_t smem_base, uint32_t bars, const float2* stats,
+                                              volatile uint32_t* ctl_go)
+{
+    using C = Cfg<D>;
+    const int lane = threadIdx.x & 31;
+    const int wq = (threadIdx.x >> 5) & 3;
+    const int row = wq * 32 + lane;
+    const bool leader = (threadIdx.x == 8 * 32);
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t stage = smem_base + C::kOffStage;
+    volatile uint32_t* go = ctl_go;   // leader's wait outcome, read by all 128 threads
+    uint32_t ph_o = 0u, ph_t = 0u;   // phase bit of tile t at bit t
+
+    for (int r = 0;; ++r) {
+        const int u = unit_at(r, p);
+        if (u < 0) break;
+        const Unit un = decode_unit(u, p);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (un.nkv[t] == 0) continue;
+            // the leader waits; one named barrier hands every thread the same
+            // outcome, so the warpgroup never splits over an abort
+            if (leader) {
+                const bool ok = ptx::mbar_wait(wc, bars + 8 * (kBarOFull + t), (ph_o >> t) & 1u,
+                                               kSiteEpilogue | (kBarOFull + t)) &&
+                                ptx::mbar_wait(wc, bars + 8 * (kBarStFull + t), (ph_t >> t) & 1u,
+                                               kSiteEpilogue | (kBarStFull + t));
+                go[0] = ok ? 1u : 0u;
+            }
+            ptx::named_bar_sync(1, 128);
+            if (go[0] == 0u) goto done;
+            ph_o ^= 1u << t;
+            ph_t ^= 1u << t;
+            ptx::tc_fence_after();
+            const float2 st = stats[t * kBM + row];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarStEmpty + t));
+            const float inv_l = 1.0f / st.x;
+            const int qrow = un.q_tile[t] * kBM + row;
+            if (qrow < p.S) p.lse[(size_t)un.bh * (size_t)p.S + (size_t)qrow] = (st.y + ptx::lg2(st.x)) * kLn2;
+            const uint32_t tO = tmem + lane_base + C::col_o(t);
+#pragma unroll 1
+            for (int box = 0; box < C::kBoxes; ++box) {
+                // the staging box is free once the previous TMA store has read it
+                if (leader) ptx::bulk_wait_read0();
+                ptx::named_bar_sync(1, 128);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32_wait(tO + box * 64 + half * 32, o);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = ptx::pack2<kBF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                                  __uint_as_float(o[2 * i + 1]) * inv_l);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int chunk = half * 4 + cc;   // 16-byte chunk of the 128-byte row
+                        const uint32_t addr = stage + row * 128 + ((chunk ^ (row & 7)) << 4);
+                        ptx::st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                    }
+                }
+                if (box == C::kBoxes - 1) {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t));
+                }
+                ptx::fence_proxy_async_shared();
+                ptx::named_bar_sync(1, 128);
+                if (leader) {
+                    ptx::tma_store_3d(tm_o, stage, box * 64, un.q_tile[t] * kBM, un.bh);
+                    ptx::bulk_commit();
+                }
+            }
+        }
+    }
+done:
+    if (leader) ptx::bulk_wait0();
+}
+
+// ---------------------------------------------------------------------------------
+// TMA producer (one thread).
+template <int D>
+__device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& wc, const CUtensorMap* tm_q,
+                                          const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t smem_base,
+                                          uint32_t bars)
+{
+    using C = Cfg<D>;
+    uint32_t ph_qe = 0u;       // phase bit of Q buffer t at bit t
+    uint32_t q_issued = 0u;    // bit t: a Q load into buffer t was issued
+    uint32_t kv_count = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int u = unit_at(r, p);
+        if (u < 0) break;
+        const Unit un = decode_unit(u, p);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (!ok || un.nkv[t] == 0) continue;
+            if (!ptx::mbar_wait(wc, bars + 8 * (kBarQEmpty + t), ((ph_qe >> t) & 1u) ^ 1u, kSiteLoad | (kBarQEmpty + t))) {
+                ok = false;
+                continue;
+            }
+            ph_qe ^= 1u << t;
+            const uint32_t fb = bars + 8 * (kBarQFull + t);
+            ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
+            const uint32_t dst = smem_base + C::kOffQ + t * C::kTileBytes;
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+                ptx::tma_load_3d(tm_q, dst + bx * C::kBoxBytes, fb, bx * 64, un.q_tile[t] * kBM, un.bh);
+            q_issued |= 1u << t;
+        }
+        for (int j = 0; j < un.nmax && ok; ++j) {
+#pragma unroll 1
+            for (int kind = 0; kind < 2; ++kind) {
+                const uint32_t idx = kv_count;
+                const uint32_t slot = idx % C::kSlots;
+                const uint32_t use = idx / C::kSlots;
+                if (!ptx::mbar_wait(wc, bars + 8 * (C::kBarKVEmpty + slot), (use & 1u) ^ 1u,
+                                    kSiteLoad | (C::kBarKVEmpty + slot))) {
+                    ok = false;
+                    break;
+                }
+                ++kv_count;
+                const uint32_t fb = bars + 8 * (kBarKVFull + slot);
+                ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
+                const uint32_t dst = smem_base + C::kOffKV + slot * C::kTileBytes;
+                const CUtensorMap* m = kind ? tm_v : tm_k;
+#pragma unroll
+                for (int bx = 0; bx < C::kBoxes; ++bx)
+                    ptx::tma_load_3d(m, dst + bx * C::kBoxBytes, fb, bx * 64, j * kBN, un.bh);
+            }
+        }
+    }
+    // Every issued copy must land before the CTA exits (after an abort, too).
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+        if ((q_issued >> t) & 1u)
+            ptx::mbar_wait_drain(wc, bars + 8 * (kBarQFull + t), ((ph_qe >> t) & 1u) ^ 1u, kSiteDrain | (kBarQFull + t));
+    for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < kv_count; ++s) {
+        const uint32_t last = kv_count - 1 - ((kv_count - 1 - s) % C::kSlots);   // last use of slot s
+        ptx::mbar_wait_drain(wc, bars + 8 * (kBarKVFull + s), (last / C::kSlots) & 1u, kSiteDrain | (kBarKVFull + s));
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// tcgen05 MMA issuer (one thread).
+template <int D, bool kBF16>
+__device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem, uint32_t smem_base,
+                                         uint32_t bars)
+{
+    using C = Cfg<D>;
+    constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);   // Q, K both K-major
+    constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, kBF16, true);      // V is MN-major (D contiguous)
+    uint32_t ph_q = 0u, ph_p = 0u, ph_oe = 0u;   // phase bit of tile t at bit t
+    uint32_t kv_count = 0;
+
+    auto kv_wait = [&](uint32_t idx) -> bool {
+        const uint32_t slot = idx % C::kSlots;
+        return ptx::mbar_wait(wc, bars + 8 * (kBarKVFull + slot), (idx / C::kSlots) & 1u,
+                              kSiteMma | (kBarKVFull + slot));
+    };
+    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + idx % C::kSlots)); };
+    // S_t = Q_t K^T: M = 128 rows, N = 128 keys, K = D in steps of 16 (32 bytes
+    // inside a 128-byte swizzled row; the next 64 columns sit in the next box).
+    auto issue_qk = [&](int t, uint32_t idx) {
+        const uint32_t qa = smem_base + C::kOffQ + t * C::kTileBytes;
+        const uint32_t kb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            ptx::mma_ss(tmem + C::col_s(t), ptx::sdesc_sw128(qa + off, 16, 1024), ptx::sdesc_sw128(kb + off, 16, 1024),
+                        kIdescQK, kk > 0 ? 1u : 0u);
+        }
+    };
+    // O_t += P_t V: A = P from TMEM (16 keys = 8 columns per step), B = V tile
+    // [128 keys x D], D contiguous: 8-key groups 1024 bytes apart, 64-column
+    // boxes kBoxBytes apart.
+    auto issue_pv = [&](int t, uint32_t idx, bool acc) {
+        const uint32_t vb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+            ptx::mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+                        ptx::sdesc_sw128(vb + kk * 16 * 128, C::kBoxBytes, 1024), kIdescPV,
+                        (acc || kk > 0) ? 1u : 0u);
+    };
+
+    for (int r = 0;; ++r) {
+        const int u = unit_at(r, p);
+        if (u < 0) break;
+        const Unit un = decode_unit(u, p);
+        const uint32_t kvb = kv_count;   // K_j is entry kvb + 2j of the ring, V_j is kvb + 2j + 1
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (un.nkv[t] == 0) continue;
+            if (!ptx::mbar_wait(wc, bars + 8 * (kBarQFull + t), (ph_q >> t) & 1u, kSiteMma | (kBarQFull + t))) goto done;
+            ph_q ^= 1u << t;
+        }
+        if (!kv_wait(kvb)) goto done;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (un.nkv[t] == 0) continue;
+            issue_qk(t, kvb);
+            ptx::mma_commit(bars + 8 * (kBarSFull + t));
+            if (un.nkv[t] == 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
+        }
+        kv_release(kvb);
+        for (int j = 0; j < un.nmax; ++j) {
+            const uint32_t iv = kvb + 2 * j + 1, ik = kvb + 2 * j + 2;
+            bool v_ready = false, k_ready = false;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (j < un.nkv[t]) {
+                    if (!ptx::mbar_wait(wc, bars + 8 * (kBarPFull + t), (ph_p >> t) & 1u, kSiteMma | (kBarPFull + t)))
+                        goto done;
+                    ph_p ^= 1u << t;
+                    if (j == 0) {
+                        // O_t is overwritten: the previous unit's epilogue must have read it
+                        if (!ptx::mbar_wait(wc, bars + 8 * (kBarOEmpty + t), ((ph_oe >> t) & 1u) ^ 1u,
+                                            kSiteMma | (kBarOEmpty + t)))
+                            goto done;
+                        ph_oe ^= 1u << t;
+                    }
+                    if (!v_ready) {
+                        if (!kv_wait(iv)) goto done;
+                        v_ready = true;
+                    }
+                    ptx::tc_fence_after();
+                    issue_pv(t, iv, j > 0);
+                    if (j == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarOFull + t));
+                }
+                if (j + 1 < un.nkv[t]) {
+                    if (!k_ready) {
+                        if (!kv_wait(ik)) goto done;
+                        k_ready = true;
+                        ptx::tc_fence_after();
+                    }
+                    issue_qk(t, ik);
+                    ptx::mma_commit(bars + 8 * (kBarSFull + t));
+                    if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
+                }
+            }
+            if (j + 1 < un.nmax) kv_release(ik);
+            kv_release(iv);
+        }
+        kv_count = kvb + 2 * un.nmax;
+    }
+done:
+    // every MMA must be complete before tensor memory is released
+    ptx::mma_commit(bars + 8 * kBarDrain);
+    ptx::mbar_wait_drain(wc, bars + 8 * kBarDrain, 0u, kSiteDrain | kBarDrain);
+}
+
+// ---------------------------------------------------------------------------------
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const Params p)
+{
+    using C = Cfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+    const uint32_t bars = base + C::kOffBars;
+    float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
+    volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(smem + C::kOffCtl);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bars + 8 * (kBarQFull + t), 1);
+            ptx::mbar_init(bars + 8 * (kBarQEmpty + t), 1);
+            ptx::mbar_init(bars + 8 * (kBarSFull + t), 1);
+            ptx::mbar_init(bars + 8 * (kBarPFull + t), 4);
+            ptx::mbar_init(bars + 8 * (kBarOFull + t), 1);
+            ptx::mbar_init(bars + 8 * (kBarOEmpty + t), 4);
+            ptx::mbar_init(bars + 8 * (kBarStFull + t), 4);
+            ptx::mbar_init(bars + 8 * (kBarStEmpty + t), 4);
+        }
+        ptx::mbar_init(bars + 8 * kBarDrain, 1);
+        for (int s = 0; s < C::kSlots; ++s) {
+            ptx::mbar_init(bars + 8 * (kBarKVFull + s), 1);
+            ptx::mbar_init(bars + 8 * (C::kBarKVEmpty + s), 1);
+        }
+        ctl[1] = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 12 && lane == 0) {
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_o);
+    }
+    if (warp == 13) {
+        ptx::tmem_alloc(base + C::kOffCtl, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = ctl[0];
+    const ptx::WaitCtx wc{base + C::kOffCtl + 4, p.timeout_ns, p.status};
+
+    if (warp < 8) {
+        ptx::setmaxnreg_inc<kRegSoftmax>();
+        softmax_role<D, kBF16>(p, wc, warp >> 2, tmem, bars, stats);
+    } else if (warp < 12) {
+        ptx::setmaxnreg_dec<kRegEpilogue>();
+        epilogue_role<D, kBF16>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
+    } else {
+        ptx::setmaxnreg_dec<kRegControl>();
+        if (warp == 12) {
+            if (lane == 0) load_role<D>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
+        } else if (warp == 13) {
+            if (lane == 0) mma_role<D, kBF16>(p, wc, tmem, base, bars);
+        }
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 13) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool kBF16>
+int launch_instance(const LaunchArgs& a, cudaStream_t stream)
+{
+    auto kern = fa_fwd_kernel<D, kBF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return (int)e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+    return (int)e;
+}
+
+}  // namespace fa

@@ -1,0 +1,333 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 fused attention forward (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one fa_fwd call over the whole workload (inputs resident in HBM).
+Metric: useful TFLOPS = 4*B*H*S^2*D / t, halved under the causal mask.  The
+default workload is the training-size causal one (4 x 32 x 4096 x 128, bf16).
+Under torchrun every rank runs its own replica of the workload (replicas only:
+the path needs no exchange between GPUs); `value` is the FLOPs of all ranks
+divided by the slowest rank's time.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on
+bounded samples of the same workload, and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from fa_inputs import WORKLOADS, make_workload  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (causal/non-causal) at 1 GB300; fraction of tensor peak"
+UNIT = "TFLOPS"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of one GPU while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        return self.summary()
+
+    def summary(self):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        loaded = [r for r in self.rows if (num(r[8]) or 0) > 0] or self.rows
+        if not loaded:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [num(r[0]) for r in loaded if num(r[0]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in loaded for n, v in zip(names, r[4:8]) if v.lower() == "active"})
+        power = [num(r[2]) for r in loaded if num(r[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(loaded[0][1]), "reasons": reasons,
+                "power_w_max": max(power) if power else None, "samples": len(loaded)}
+
+
+def oracle_rows_sample(w, q, k, v, n_rows, seed):
+    """(heads, rows, useful FLOPs) of a sample of rows of the workload."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    BH, S = w.B * w.H, w.S
+    heads = rng.integers(0, BH, n_rows)
+    rows = rng.integers(0, S, n_rows)
+    keys = (rows + 1) if w.causal else np.full(n_rows, S)
+    flops = float(4.0 * w.D * keys.sum())     # QK^T and PV over the keys each row sees
+    return heads, rows, flops
+
+
+def time_oracle(w, q, k, v, budget_s: float, steps: int, seed: int = 0):
+    """Run the fp64 oracle (row-by-row definition) on `steps` bounded samples;
+    returns (TFLOPS, seconds per step, sample description, threads)."""
+    import numpy as np
+    import oracle
+    from fa_inputs import to_f64
+    nthreads = os.cpu_count() or 1
+    # the oracle reads a few heads only: gather them once (exact fp64 widening)
+    BH, S, D = w.B * w.H, w.S, w.D
+    qf, kf, vf = (x.reshape(BH, S, D) for x in (q, k, v))
+    # calibrate rows per step so one step takes about budget_s seconds
+    n_rows = max(nthreads, 8)
+    per_step = []
+    tflops = []
+    desc = None
+    for step in range(steps + 1):
+        heads, rows, flops = oracle_rows_sample(w, q, k, v, n_rows, seed + step)
+        uh, inv = np.unique(heads, return_inverse=True)
+        sel = torch.from_numpy(uh)
+        sub = lambda x: to_f64(x[sel].unsqueeze(0))
+        qs, ks, vs = sub(qf), sub(kf), sub(vf)
+        t0 = time.perf_counter()
+        oracle.attention_rows(qs, ks, vs, w.causal, w.scale, inv, rows, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        if step == 0:
+            # calibration step: resize the sample to the budget, not timed
+            n_rows = max(nthreads, int(n_rows * budget_s / max(dt, 1e-3)))
+            continue
+        per_step.append(dt)
+        tflops.append(flops / dt / 1e12)
+        desc = (f"{n_rows} random (head, row) pairs of the {w.name} workload per step, "
+                f"fp64 row-by-row definition, {nthreads} OpenMP threads")
+    return statistics.median(tflops), statistics.median(per_step), desc, nthreads
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    q, k, v = make_workload(w)
+    budget = max(0.05, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    value, sec, desc, cores = time_oracle(w, q, k, v, budget, args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+                   "causal": w.causal, "input_dtype": w.dtype},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import attention_fa_fwd_gb300 as fa
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the kernel has no CPU path)")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    fa.build()
+    dev = torch.device("cuda", local)
+    q, k, v = make_workload(w, seed=rank)
+    qd, kd, vd = (x.to(dev) for x in (q, k, v))
+    od = torch.empty_like(qd)
+    ld = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+    info = fa.launch_info(w.B, w.H, w.S, w.D, w.causal, qd.dtype)
+
+    def step():
+        fa.fa_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    status, site = fa.device_status(clear=True, stream=stream)
+    if status != fa.FA_OK:
+        raise SystemExit(f"in-kernel wait gave up at site {site:#x}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    status, site = fa.device_status(clear=True, stream=stream)
+    if status != fa.FA_OK:
+        raise SystemExit(f"in-kernel wait gave up at site {site:#x}")
+    t = torch.tensor([ms], device=dev, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    flops = w.flops()
+    value = flops * world / (ms_step * 1e-3) / 1e12
+
+    # end to end through the C ABI with host buffers: H2D of q, k, v, the
+    # kernel, D2H of o and lse, every step
+    qh, kh, vh = (x.pin_memory() for x in (q, k, v))
+    oh = torch.empty_like(qh).pin_memory()
+    lh = torch.empty((w.B, w.H, w.S), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        fa.fa_fwd_hostio(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, causal=w.causal, scale=w.scale,
+                         stream=stream)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    te = torch.tensor([e0.elapsed_time(e1) / e2e_steps], device=dev, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = flops * world / (float(te.item()) * 1e-3) / 1e12
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    pk, pk_kind = peaks()
+    peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms_step * 1e-3) / 1e12   # one launch per step on this stream
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "fp16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs (Q,K,V,O = %d MiB) exceed the 129 MB L2; no flush" %
+                         (4 * q.numel() * q.element_size() >> 20),
+                   "grid": info["grid"], "tiles_per_unit": info["tiles_per_unit"],
+                   "units": info["units"]},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"bf16 dense burst ({pk_kind})", "traffic": args.traffic},
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * world,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        budget = 15.0
+        cv, _, desc, cores = time_oracle(w, q, k, v, budget, 1)
+        line["cpu_baseline"] = {"value": round(cv, 6), "unit": UNIT, "cores": cores,
+                                "kind": "oracle", "sample": desc}
+    elif not args.no_cpu_baseline:
+        line["cpu_baseline"] = None
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="train_causal", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of the current kernel")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

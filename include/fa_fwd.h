@@ -1,0 +1,148 @@
+/*
+ * fa_fwd.h - C ABI of the GB300 (sm_103a) fused attention forward pass.
+ *
+ * The operation (one call = the whole hot path):
+ *
+ *   O    = softmax(Q K^T * scale + mask) V
+ *   LSE_i = ln sum_j exp(scale * q_i . k_j)      over the keys j row i may see
+ *
+ * for every (batch b, head h) independently.  The formula is the one of
+ * "CUDA手写masked multi-head attention", section 3.1 (Attention公式的CUDA语义
+ * 重写); the causal mask keeps the lower triangle (key j <= query i), as the
+ * same section's mask code and comment state, and masked scores count as -inf.
+ * The computation is tiled with online softmax ("FlashAttention的Triton性能考古学",
+ * sections 核心算法回顾 and 关键优化：反转循环顺序: running max and sum per row,
+ * one normalisation at the end), so the S x S score matrix never reaches device
+ * memory, and uses the conditional rescale of "G6: Cluster 与 2CTA 探索", V41,
+ * so O is rescaled only when a row's maximum rises by more than 2^8.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout     q, k, v, o: contiguous [B, H, S, D] tensors of `dtype` (row-major,
+ *            D fastest).  lse: contiguous [B, H, S] float32.  Q, K and V share
+ *            S (self-attention, square mask).
+ * Pointers   "device" pointers must be addressable by the current CUDA device
+ *            (cudaMalloc / torch CUDA tensors); "host" pointers are ordinary or
+ *            pinned host memory.  All tensor pointers must be 16-byte aligned.
+ * Ownership  The caller allocates and frees every buffer.  The library
+ *            allocates no device memory and keeps no per-call state; it caches
+ *            one function-attribute setting and the SM count per device.
+ * Streams    `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *            stream).  Work is enqueued on it and the call returns without
+ *            synchronising; calls on different streams may run concurrently.
+ * Errors     Every entry point returns an fa_status_t and never aborts, throws
+ *            or prints.  Invalid arguments are rejected before anything is
+ *            enqueued.
+ * Sizes      B, H, S >= 1 with B*H*S*D < 2^31 elements per tensor; D in {64,
+ *            128}; dtype fp16 or bf16; any S (tails are masked in the kernel).
+ */
+#ifndef FA_FWD_H
+#define FA_FWD_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_DTYPE_F16 = 0,   /* IEEE binary16 inputs and output, fp32 accumulation */
+    FA_DTYPE_BF16 = 1   /* bfloat16 inputs and output, fp32 accumulation */
+} fa_dtype_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null pointer, B/H/S < 1, causal not 0/1, scale not finite or <= 0,
+                                sizes overflowing 2^31 elements */
+    FA_ERR_UNSUPPORTED = 2,  /* D not in {64, 128}, unknown dtype, no sm_100-family device */
+    FA_ERR_MISALIGNED = 3,   /* a tensor pointer not 16-byte aligned */
+    FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, copy, tensor map) */
+    FA_ERR_TIMEOUT = 5       /* a bounded in-kernel wait gave up (reported by fa_device_status) */
+} fa_status_t;
+
+/*
+ * fa_fwd - the fused attention forward pass on device buffers.
+ *
+ *   q, k, v  device, read-only, [B, H, S, D] of dtype
+ *   o        device, written, [B, H, S, D] of dtype; O rounded to nearest-even
+ *   lse      device, written, [B, H, S] float32, natural log of the row sums of
+ *            exp(scaled scores) over the allowed keys
+ *   causal   0 = no mask, 1 = key j allowed for query i iff j <= i
+ *   scale    multiplier of Q K^T, finite and > 0 (usually 1/sqrt(D))
+ *   dtype    an fa_dtype_t
+ *   stream   cudaStream_t as void*
+ *
+ * One kernel launch per call.  o and lse must not overlap q, k or v.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int S, int D, int causal, float scale, int dtype, void* stream);
+
+/*
+ * fa_fwd_hostio - the same pass with host-side inputs and outputs.
+ *
+ * Enqueues on `stream`: host->device copies of q_h, k_h, v_h into the caller's
+ * device buffers q_d, k_d, v_d; fa_fwd on them into o_d, lse_d; device->host
+ * copies of o_d, lse_d into o_h, lse_h.  Returns once everything is enqueued;
+ * the caller synchronises `stream` before reading o_h / lse_h.  Host buffers
+ * should be pinned for the copies to be asynchronous.  Same layouts, sizes and
+ * errors as fa_fwd; all ten pointers must be non-null and 16-byte aligned.
+ */
+int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                  void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
+                  int B, int H, int S, int D, int causal, float scale, int dtype, void* stream);
+
+/* Launch geometry fa_fwd would use for a problem on the current device. */
+typedef struct {
+    int grid;            /* CTAs launched (persistent: <= SM count) */
+    int block;           /* threads per CTA */
+    int smem_bytes;      /* dynamic shared memory per CTA */
+    int tiles_per_unit;  /* 128-row query tiles per work unit (1 or 2) */
+    int units;           /* work units = B*H * ceil(query tiles / tiles_per_unit) */
+    int head_group;      /* heads scheduled together (longest units first within a group) */
+    int num_sms;         /* SM count of the current device */
+} fa_launch_info_t;
+
+/*
+ * fa_fwd_launch_info - fills *info for fa_fwd(B, H, S, D, causal, dtype).
+ * Host only: queries the current device's SM count, launches nothing.
+ * Errors as fa_fwd's argument checks (pointers are not examined).
+ */
+int fa_fwd_launch_info(int B, int H, int S, int D, int causal, int dtype, fa_launch_info_t* info);
+
+/*
+ * fa_fwd_plan - the same geometry for a device with `num_sms` SMs (>= 1).
+ * Pure host computation: touches no device, so it works without a GPU.
+ */
+int fa_fwd_plan(int B, int H, int S, int D, int causal, int dtype, int num_sms, fa_launch_info_t* info);
+
+/*
+ * fa_device_status - status word of the bounded in-kernel waits.
+ *
+ * Every wait inside the kernels gives up after a time limit (default 4 s,
+ * FA_WAIT_TIMEOUT_MS overrides it when the library is loaded), records the
+ * wait site in a device status word and makes its CTA exit cleanly.  This call
+ * synchronises `stream`, reads the word, clears it if `clear` is non-zero and
+ * returns FA_OK or FA_ERR_TIMEOUT; *site (if non-null) receives the recorded
+ * site code (0 = none).  FA_ERR_CUDA if the synchronisation fails.
+ */
+int fa_device_status(void* stream, int clear, unsigned int* site);
+
+/*
+ * fa_selftest_wait_timeout - exercises the bounded wait used by the kernels.
+ *
+ * Launches one CTA that waits on a shared-memory barrier nothing ever arrives
+ * on, with a limit of `timeout_us` microseconds (1..10^7).  The wait gives up,
+ * records its site in the status word and the kernel returns.  Returns FA_OK
+ * once enqueued; read the outcome with fa_device_status.  Faults and hangs
+ * nothing: the context stays usable.
+ */
+int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream);
+
+/* Human-readable text for an fa_status_t; never NULL. */
+const char* fa_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_FWD_H */

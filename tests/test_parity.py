@@ -1,0 +1,109 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the fp64 oracle,
+element by element, on seeded inputs.  Tolerances: max|dO| <= 4e-3 (fp16) or
+1.6e-2 (bf16), max|dLSE| <= 1e-3."""
+import pytest
+import torch
+
+import attention_fa_fwd_gb300 as fa
+from fa_inputs import WORKLOADS, make_qkv
+from parity_util import check_full, check_sampled, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    fa.build()
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_causal"])
+def test_tiny_workload(name):
+    w = WORKLOADS[name]
+    check_full(w.B, w.H, w.S, w.D, w.dtype, w.causal)
+
+
+SHAPES = [
+    # B, H, S, D  (several tiles, ragged tails, one-row and one-tile cases)
+    (1, 1, 1, 64), (1, 1, 1, 128), (1, 2, 17, 64), (2, 3, 127, 128), (1, 2, 129, 64),
+    (2, 2, 200, 128), (1, 3, 256, 64), (1, 2, 257, 128), (2, 2, 389, 64), (1, 2, 640, 128),
+]
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,S,D", SHAPES)
+def test_shapes(B, H, S, D, dtype, causal):
+    check_full(B, H, S, D, dtype, causal, seed=B * 1000 + S)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_heads_two_tiles_per_unit(causal):
+    # enough query tiles that units hold two tiles (ping-pong path), odd tile count
+    check_full(2, 80, 384, 64, "fp16", causal, seed=5)
+    check_full(1, 160, 300, 128, "bf16", causal, seed=6)
+
+
+def test_batch1_causal_workload_full():
+    w = WORKLOADS["batch1_causal"]
+    check_full(w.B, w.H, w.S, w.D, w.dtype, w.causal)
+
+
+@pytest.mark.parametrize("name", ["wide_noncausal", "train_causal", "stress_causal"])
+def test_full_size_workload_sampled(name):
+    w = WORKLOADS[name]
+    check_sampled(w.B, w.H, w.S, w.D, w.dtype, w.causal, kind=w.kind)
+
+
+def test_long_sequence_sampled():
+    check_sampled(1, 2, 32768 + 77, 128, "bf16", True)
+
+
+def test_causal_row0_is_v0_exactly():
+    for D, dtype in ((64, "fp16"), (128, "bf16")):
+        q, k, v = make_qkv(2, 3, 300, D, dtype, seed=3)
+        o, _ = run_gpu(q, k, v, True, 1.0 / D ** 0.5)
+        assert torch.equal(o[:, :, 0], v[:, :, 0])
+
+
+def test_identical_keys_give_mean_of_v():
+    q, k, v = make_qkv(1, 2, 256, 128, "bf16", seed=4)
+    k = k[:, :, :1].expand_as(k).contiguous()
+    o, _ = run_gpu(q, k, v, False, 0.1)
+    want = v.double().mean(dim=2, keepdim=True).expand_as(o)
+    assert (o.double() - want).abs().max().item() < 1.6e-2
+
+
+def test_deterministic_and_stream_ordered():
+    q, k, v = make_qkv(1, 8, 1000, 128, "bf16", seed=7)
+    s = torch.cuda.Stream()
+    a = run_gpu(q, k, v, True, 0.09)
+    b = run_gpu(q, k, v, True, 0.09, stream=s)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_hostio_matches_device_path():
+    q, k, v = make_qkv(2, 4, 333, 64, "fp16", seed=8)
+    want_o, want_l = run_gpu(q, k, v, True, 0.125)
+    qh, kh, vh = (x.pin_memory() for x in (q, k, v))
+    oh = torch.empty_like(qh).pin_memory()
+    lh = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
+    qd, kd, vd, od = (torch.empty_like(q, device="cuda") for _ in range(4))
+    ld = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    fa.fa_fwd_hostio(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, causal=True, scale=0.125)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, want_o) and torch.equal(lh, want_l)
+
+
+def test_rejected_call_launches_nothing():
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 128, 64, "fp16"))
+    o = torch.full_like(q, 7.0)
+    lse = torch.full(q.shape[:3], 7.0, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd(q, k, v, scale=-1.0, out=o, lse=lse)
+    assert e.value.status == fa.FA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert (o == 7.0).all() and (lse == 7.0).all()
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q.transpose(1, 2), k, v)
