@@ -40,7 +40,7 @@ class FaError(RuntimeError):
 class LaunchInfo(ctypes.Structure):
     _fields_ = [("grid", ctypes.c_int), ("block", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("tiles_per_unit", ctypes.c_int), ("units", ctypes.c_int),
-                ("head_group", ctypes.c_int), ("num_sms", ctypes.c_int)]
+                ("head_group", ctypes.c_int), ("num_sms", ctypes.c_int), ("schedule", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

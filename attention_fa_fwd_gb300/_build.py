@@ -16,6 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa_fwd.so")
+TRACE_LIB = os.path.join(PKG, "libfa_fwd_trace.so")
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 
@@ -32,16 +33,16 @@ def _inputs():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+def is_stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def _compile(src: str, ptxas_verbose: bool) -> tuple[str, str]:
-    obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
-    cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, ptxas_verbose: bool, trace: bool = False) -> tuple[str, str]:
+    obj = os.path.join(OBJDIR, os.path.basename(src) + (".trace.o" if trace else ".o"))
+    cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj] + (["-DFA_TRACE"] if trace else [])
     if ptxas_verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -50,28 +51,31 @@ def _compile(src: str, ptxas_verbose: bool) -> tuple[str, str]:
     return obj, r.stderr
 
 
-def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None) -> str:
-    """Compile every CUDA translation unit and link libfa_fwd.so; returns its path."""
-    if not force and not ptxas_verbose and not is_stale():
-        return LIB
+def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None,
+          trace: bool = False) -> str:
+    """Compile every CUDA translation unit and link libfa_fwd.so (or, with
+    trace=True, the event-tracing variant libfa_fwd_trace.so); returns its path."""
+    lib = TRACE_LIB if trace else LIB
+    if not force and not ptxas_verbose and not is_stale(lib):
+        return lib
     os.makedirs(OBJDIR, exist_ok=True)
     srcs = sources()
     with ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
-        results = list(ex.map(lambda s: _compile(s, ptxas_verbose), srcs))
+        results = list(ex.map(lambda s: _compile(s, ptxas_verbose, trace), srcs))
     if ptxas_verbose:
         for _, log in results:
             if log.strip():
                 print(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [NVCC, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
            "-Xlinker", f"-rpath,{os.path.join(CUDA_HOME, 'lib64')}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force=True, ptxas_verbose="-v" in sys.argv))
+    print(build(force=True, ptxas_verbose="-v" in sys.argv, trace="--trace" in sys.argv))

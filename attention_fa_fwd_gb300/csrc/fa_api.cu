@@ -5,6 +5,8 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -20,6 +22,12 @@ using fa::kBM;
 
 // Device status word: a bounded wait that gives up stores its site here.
 __device__ unsigned int g_fa_status = 0u;
+
+#ifdef FA_TRACE
+// Trace buffer of the FA_TRACE build, set with fa_trace_set.
+unsigned long long* g_trace = nullptr;
+int g_trace_ctas = 0, g_trace_cap = 0;
+#endif
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_num_sms[kMaxDevices];     // 0 = not queried yet
@@ -87,6 +95,76 @@ int check_args(int B, int H, int S, int D, int causal, int dtype)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---- causal schedule planner ------------------------------------------------
+// The kernel walks a list of work units ordered group by group (`head_group`
+// heads per group), longest first inside a group, CTA c taking entries in snake
+// order (see unit_at / decode_unit in fa_fwd_kernel.cuh).  Larger groups balance
+// the causal triangle better; smaller groups keep the K/V of the heads in flight
+// within L2.  The planner replays the assignment for every group size whose K/V
+// fits the budget and keeps the best-balanced one (the smallest such group
+// within 0.5% of the best).  Results are cached per shape.
+
+constexpr long long kGroupKVBudget = 160ll << 20;   // bytes of K/V per group of heads
+
+// Load of the most loaded CTA over the mean, with the cost of a unit taken as
+// its key tiles plus a fixed per-unit overhead of two tiles.
+double snake_imbalance(int BH, int n_qtiles, int tpu, int n_qgroups, long long units, int grid, int hg,
+                       std::vector<double>& load)
+{
+    load.assign((size_t)grid, 0.0);
+    const long long per_group = (long long)hg * n_qgroups;
+    double total = 0.0;
+    for (long long u = 0; u < units; ++u) {
+        const long long r = u / grid, pos = u % grid;
+        const long long c = (r & 1) ? (grid - 1 - pos) : pos;
+        const long long g = u / per_group, w = u - g * per_group;
+        const long long h0 = g * hg;
+        const long long hgg = hg < BH - h0 ? hg : BH - h0;
+        const long long rank = w / hgg;
+        const long long qg = n_qgroups - 1 - rank;
+        double cost = 2.0;
+        for (int t = 0; t < tpu; ++t) {
+            const long long qt = qg * tpu + t;
+            if (qt < n_qtiles) cost += (double)(qt + 1);
+        }
+        load[(size_t)c] += cost;
+        total += cost;
+    }
+    double mx = 0.0;
+    for (double x : load) mx = x > mx ? x : mx;
+    return mx / (total / grid);
+}
+
+int plan_head_group(int BH, int S, int D, int n_qtiles, int tpu, int n_qgroups, long long units, int grid)
+{
+    struct Entry { int BH, S, D, grid, hg; };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry& e : cache)
+            if (e.BH == BH && e.S == S && e.D == D && e.grid == grid) return e.hg;
+    }
+    const long long kv_head_bytes = 2ll * S * D * 2;
+    long long cap = kGroupKVBudget / kv_head_bytes;
+    if (cap < 1) cap = 1;
+    if (cap > BH) cap = BH;
+    std::vector<double> load;
+    std::vector<double> score((size_t)cap + 1, 0.0);
+    double best = 1e30;
+    for (int hg = 1; hg <= cap; ++hg) {
+        score[(size_t)hg] = snake_imbalance(BH, n_qtiles, tpu, n_qgroups, units, grid, hg, load);
+        if (score[(size_t)hg] < best) best = score[(size_t)hg];
+    }
+    int pick = (int)cap;
+    for (int hg = 1; hg <= cap; ++hg)
+        if (score[(size_t)hg] <= best + 0.005) { pick = hg; break; }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() >= 256) cache.erase(cache.begin());
+    cache.push_back({BH, S, D, grid, pick});
+    return pick;
+}
+
 // Work-unit geometry (see the schedule comment in fa_fwd_kernel.cuh).
 void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t* info, fa::Params* p)
 {
@@ -98,14 +176,14 @@ void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t*
     const int n_qgroups = (n_qtiles + tpu - 1) / tpu;
     const long long units = (long long)BH * n_qgroups;
     const int grid = (int)(units < num_sms ? units : num_sms);
-    int head_group = 1;
-    if (causal) {
-        // a group holds about two rounds of units, so the snake order pairs each
-        // long unit with a short one
-        head_group = (int)((2ll * grid + n_qgroups / 2) / n_qgroups);
-        if (head_group < 1) head_group = 1;
-        if (head_group > BH) head_group = BH;
-    }
+    // Causal units differ in cost.  With more than one round of units, pair
+    // each query group with its mirror (equal cost per pair, and the pair shares
+    // its head's K/V in L2); with a single round every CTA takes one unit.
+    // Without the mask every unit costs the same and heads simply go in order.
+    const bool pairs = causal && units > grid;
+    const int head_group =
+        (causal && !pairs) ? plan_head_group(BH, S, D, n_qtiles, tpu, n_qgroups, units, grid) : 1;
+    const int pairs_per_head = (n_qgroups + 1) / 2;
     if (info) {
         info->grid = grid;
         info->block = fa::kThreads;
@@ -114,6 +192,7 @@ void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t*
         info->units = (int)units;
         info->head_group = head_group;
         info->num_sms = num_sms;
+        info->schedule = pairs ? 1 : 0;
     }
     if (p) {
         p->BH = BH;
@@ -123,7 +202,10 @@ void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t*
         p->tpu = tpu;
         p->n_qgroups = n_qgroups;
         p->n_units = (int)units;
+        p->sched = pairs ? fa::kSchedPairs : fa::kSchedSnake;
         p->head_group = head_group;
+        p->pairs_per_head = pairs_per_head;
+        p->n_pairs = (long long)BH * pairs_per_head;
         p->causal = causal;
         p->mask_last = (causal || (S % fa::kBN) != 0) ? 1 : 0;
     }
@@ -209,6 +291,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     a.p.lse = lse;
     a.p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.p.timeout_ns = timeout_ns();
+    a.p.trace = nullptr;
+    a.p.trace_ctas = 0;
+    a.p.trace_cap = 0;
+#ifdef FA_TRACE
+    a.p.trace = g_trace;
+    a.p.trace_ctas = g_trace_ctas;
+    a.p.trace_cap = g_trace_cap;
+#endif
     void* status = nullptr;
     if (cudaGetSymbolAddress(&status, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
     a.p.status = static_cast<unsigned int*>(status);
@@ -274,5 +364,18 @@ int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream)
                                            static_cast<cudaStream_t>(stream));
     return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+#ifdef FA_TRACE
+// Trace build only: every later fa_fwd records events of CTAs [0, ctas) into
+// `buf` (device, ctas * 5 * cap 64-bit words, caller-owned, zeroed by the caller).
+int fa_trace_set(unsigned long long* buf, int ctas, int cap)
+{
+    if ((buf == nullptr) != (ctas == 0) || ctas < 0 || cap < 0) return FA_ERR_INVALID_ARG;
+    g_trace = buf;
+    g_trace_ctas = ctas;
+    g_trace_cap = cap;
+    return FA_OK;
+}
+#endif
 
 }  // extern "C"

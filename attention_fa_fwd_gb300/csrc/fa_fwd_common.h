@@ -23,11 +23,41 @@ struct Params {
     int tpu;                    // query tiles per work unit: 1 or 2
     int n_qgroups;              // ceil(n_qtiles / tpu)
     int n_units;                // BH * n_qgroups
-    int head_group;             // heads whose units are interleaved, longest first
+    int sched;                  // kSchedSnake or kSchedPairs
+    int head_group;             // snake: heads whose units are interleaved, longest first
+    int pairs_per_head;         // pairs: ceil(n_qgroups / 2)
+    long long n_pairs;          // pairs: BH * pairs_per_head
     int causal;                 // 1: key j allowed for query i iff j <= i
     int mask_last;              // the last K/V tile of a query tile needs masking
     float scale_log2;           // scale * log2(e)
+    // Event trace (used only by the FA_TRACE build): per traced CTA and role,
+    // `trace_cap` 64-bit records of event, argument and SM clock.
+    unsigned long long* trace;
+    int trace_ctas;
+    int trace_cap;
 };
+
+// Trace roles and events (FA_TRACE build).  A record is
+// event << 56 | (arg & 0xFFFF) << 40 | (clock64 & (2^40 - 1)).
+enum TraceRole : int { kTrSoftmax0 = 0, kTrSoftmax1 = 1, kTrEpilogue = 2, kTrLoad = 3, kTrMma = 4, kTraceRoles = 5 };
+enum TraceEvent : unsigned {
+    kEvSReady = 1,      // softmax: scores of key tile j visible (arg j)
+    kEvPDone = 2,       // softmax: P of key tile j published (arg j)
+    kEvRescale = 3,     // softmax: O rescaled in TMEM (arg j)
+    kEvSLoaded = 4,     // softmax: scores in registers (arg j)
+    kEvMaxDone = 5,     // softmax: row maximum and re-base decision done (arg j)
+    kEvExpDone = 6,     // softmax: all P stores issued (arg j)
+    kEvUnit = 10,       // MMA: unit starts (arg unit index)
+    kEvQK = 11,         // MMA: QK issued (arg t << 12 | j)
+    kEvPV = 12,         // MMA: PV issued (arg t << 12 | j)
+    kEvPWait = 13,      // MMA: starts waiting for P (arg t << 12 | j)
+    kEvQLoad = 20,      // load: Q tile issued (arg t)
+    kEvKVLoad = 21,     // load: K or V tile issued (arg ring index)
+    kEvOFull = 30,      // epilogue: O of tile t complete (arg t)
+    kEvEpiDone = 31,    // epilogue: tile t stored (arg t)
+};
+
+enum : int { kSchedSnake = 0, kSchedPairs = 1 };
 
 struct LaunchArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;

@@ -12,8 +12,8 @@
 // CTA layout (512 threads, one CTA per SM, persistent over work units):
 //   warps 0-3   softmax warpgroup of query tile 0 (one thread per row)
 //   warps 4-7   softmax warpgroup of query tile 1
-//   warps 8-11  correction/epilogue warpgroup: O / l, LSE, bf16/fp16 convert,
-//               shared-memory staging and TMA store
+//   warps 8-11  correction/epilogue warpgroup: the final correction O / l,
+//               LSE, bf16/fp16 convert, shared-memory staging and TMA store
 //   warp 12     TMA producer: Q tiles, then a ring of K/V slots
 //   warp 13     tcgen05 MMA issuer (one thread) and TMEM owner
 //   warps 14-15 idle (they complete the fourth warpgroup for setmaxnreg)
@@ -27,14 +27,20 @@
 // MMA issue order per key tile j ("G6", V39, interleave):
 //   PV0(j), QK0(j+1), PV1(j), QK1(j+1)
 // so the tensor core computes one tile's scores while the other tile's softmax
-// runs.  Because tcgen05.commit covers every earlier MMA of the issuing thread,
-// the commit that announces S_t(j+1) also guarantees PV_t(j) has finished, so
-// the softmax warpgroup may rescale O_t in TMEM right after it sees S_t(j+1).
+// runs.  Each PV is issued in two halves (keys 0-63, then 64-127): the softmax
+// publishes the first half of P before it computes the second ("G6", V43, PV
+// split), so half of P*V overlaps the second half of the exponentials.
 //
 // Softmax uses the conditional rescale of "G6", V41, in the base-2 domain: the
 // row base b only moves when the tile maximum exceeds b + 8, so p = 2^(x - b)
-// lies in (0, 256] and O is rescaled (by the warp that owns the rows, only when
-// a row of that warp moved; "G6", V41/V44) in the rare re-base case.
+// lies in (0, 256].  The row maximum of an unmasked tile comes with the TMEM
+// load (tcgen05.ld.red .max; "G6", V41: "4 ld.red").  When a row's base moves,
+// the softmax warp owning it rescales its 32 rows of O in TMEM before it
+// publishes P ("G6", V44: the rescale moved into the softmax warpgroups; here
+// too a separate correction handshake measured ~16% slower).  Because
+// tcgen05.commit covers every earlier MMA of the issuing thread, the commit
+// that announces S_t(j) also guarantees PV_t(j-1) has finished, so O_t is
+// stable when the softmax rescales it.
 //
 // Causal masking: with 128 x 128 tiles a query tile's diagonal is exactly its
 // last key tile; later key tiles are skipped, only the diagonal tile (and a
@@ -54,23 +60,28 @@ namespace fa {
 constexpr float kRebaseThreshold = 8.0f;   // log2 units ("G6", V41: base + 8)
 constexpr float kLn2 = 0.693147180559945309f;
 
-// Register budget per warpgroup after setmaxnreg (sum = 512 for 512 threads at 128).
-constexpr uint32_t kRegSoftmax = 176;
-constexpr uint32_t kRegEpilogue = 64;
-constexpr uint32_t kRegControl = 96;
+// Register budget per warpgroup after setmaxnreg: softmax x2, epilogue, control
+// (load + MMA).  The four add up to 512 = 65536 registers / 128 threads; the
+// splits are the spill-free ones ptxas -v reports for each head dim.
+template <int D> struct RegSplit;
+template <> struct RegSplit<128> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 56, kControl = 104; };
+template <> struct RegSplit<64> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 72, kControl = 88; };
+static_assert(2 * RegSplit<128>::kSoftmax + RegSplit<128>::kEpilogue + RegSplit<128>::kControl == 512, "");
+static_assert(2 * RegSplit<64>::kSoftmax + RegSplit<64>::kEpilogue + RegSplit<64>::kControl == 512, "");
 
 // Barrier indices inside the barrier array.
 enum : int {
     kBarQFull = 0,      // [2] Q tile t landed (TMA tx)
     kBarQEmpty = 2,     // [2] last QK of tile t finished (commit)
     kBarSFull = 4,      // [2] scores S_t ready (commit)
-    kBarPFull = 6,      // [2] P_t written to TMEM, O_t corrected (4 softmax warps)
-    kBarOFull = 8,      // [2] last PV of tile t finished (commit)
-    kBarOEmpty = 10,    // [2] epilogue done reading O_t (4 epilogue warps)
-    kBarStFull = 12,    // [2] row statistics of tile t in shared memory (4 softmax warps)
-    kBarStEmpty = 14,   // [2] epilogue took the statistics (4 epilogue warps)
-    kBarDrain = 16,     // MMA drain at exit (commit)
-    kBarKVFull = 17,    // [slots] K or V tile landed (TMA tx)
+    kBarPHalf = 6,      // [2] P_t keys 0-63 in TMEM, O_t rescaled (4 softmax warps)
+    kBarPFull = 8,      // [2] P_t keys 64-127 in TMEM (4 softmax warps)
+    kBarOFull = 10,     // [2] last PV of tile t finished (commit)
+    kBarOEmpty = 12,    // [2] epilogue done reading O_t (4 epilogue warps)
+    kBarStFull = 14,    // [2] row statistics of tile t in shared memory (4 softmax warps)
+    kBarStEmpty = 16,   // [2] epilogue took the statistics (4 epilogue warps)
+    kBarDrain = 18,     // MMA drain at exit (commit)
+    kBarKVFull = 19,    // [slots] K or V tile landed (TMA tx)
 };
 
 template <int D>
@@ -95,35 +106,57 @@ struct Cfg {
 };
 
 struct Unit {
+    int id;          // position of the unit in the schedule (trace only)
     int bh;
     int q_tile[2];   // query tile index of each tile of the unit
     int nkv[2];      // key tiles to visit per tile (0 = tile absent)
     int nmax;
 };
 
-// Work units are ordered group of `head_group` heads by group; inside a group
-// the longest units (causal: the last query tiles) come first.  CTA c takes, in
-// round r, entry r*G + c (r even) or r*G + G-1-c (r odd): a snake over a list of
-// falling cost, which evens out the causal triangle, and heads of one group run
-// together so their K/V stay in L2.
-__device__ __forceinline__ int unit_at(int r, const Params& p)
+enum : int { kUnitDone = 0, kUnitOk = 1, kUnitSkip = 2 };
+
+// The r-th work unit of this CTA; every role of the CTA walks the same list.
+//
+// kSchedSnake: units ordered group of `head_group` heads by group, longest
+// first inside a group (causal: the last query tiles); CTA c takes, in round r,
+// entry r*G + c (r even) or r*G + G-1-c (r odd), a snake over a list of falling
+// cost.  Without the mask (all units cost the same) the group is one head and
+// consecutive CTAs share a head's K/V.
+//
+// kSchedPairs (causal): query group g of a head is paired with group
+// n_qgroups-1-g, so every pair costs the same; CTA c takes pair (r/2)*G + c, its
+// long unit on even r and its short unit on odd r.  Pairs are ordered head by
+// head, so the CTAs of a round share few heads and the short unit re-reads K/V
+// the long one just brought into L2.  With an odd group count the middle group
+// pairs with itself and its second slot is skipped.
+__device__ __forceinline__ int unit_at(int r, const Params& p, Unit& un)
 {
     const long long G = gridDim.x, c = blockIdx.x;
-    const long long u = (long long)r * G + ((r & 1) ? (G - 1 - c) : c);
-    return u < p.n_units ? (int)u : -1;
-}
-
-__device__ __forceinline__ Unit decode_unit(int u, const Params& p)
-{
-    const int per_group = p.head_group * p.n_qgroups;
-    const int g = u / per_group;
-    const int w = u - g * per_group;
-    const int h0 = g * p.head_group;
-    const int hg = min(p.head_group, p.BH - h0);
-    const int rank = w / hg;
-    Unit un;
-    un.bh = h0 + (w - rank * hg);
-    const int qg = p.causal ? (p.n_qgroups - 1 - rank) : rank;
+    int bh, qg;
+    if (p.sched == kSchedPairs) {
+        const long long pi = (long long)(r >> 1) * G + c;
+        if (pi >= p.n_pairs) return kUnitDone;
+        const int h = (int)(pi / p.pairs_per_head);
+        const int k = (int)(pi - (long long)h * p.pairs_per_head);
+        const int longer = p.n_qgroups - 1 - k;
+        if ((r & 1) && k == longer) return kUnitSkip;
+        bh = h;
+        qg = (r & 1) ? k : longer;
+        un.id = (int)(2 * pi + (r & 1));
+    } else {
+        const long long u = (long long)r * G + ((r & 1) ? (G - 1 - c) : c);
+        if (u >= p.n_units) return kUnitDone;
+        const int per_group = p.head_group * p.n_qgroups;
+        const int g = (int)u / per_group;
+        const int w = (int)u - g * per_group;
+        const int h0 = g * p.head_group;
+        const int hg = min(p.head_group, p.BH - h0);
+        const int rank = w / hg;
+        bh = h0 + (w - rank * hg);
+        qg = p.causal ? (p.n_qgroups - 1 - rank) : rank;
+        un.id = (int)u;
+    }
+    un.bh = bh;
     un.nmax = 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -133,8 +166,30 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params& p)
         un.nkv[t] = active ? (p.causal ? min(qt + 1, p.n_kv) : p.n_kv) : 0;
         un.nmax = max(un.nmax, un.nkv[t]);
     }
-    return un;
+    return kUnitOk;
 }
+
+// Event trace: compiled in only with -DFA_TRACE (a separate library); the
+// production kernel contains none of it.
+#ifdef FA_TRACE
+__device__ __forceinline__ void trace_event(const Params& p, int role, uint32_t& n, uint32_t ev, uint32_t arg)
+{
+    if ((int)blockIdx.x < p.trace_ctas && (int)n < p.trace_cap) {
+        const unsigned long long t = clock64();
+        p.trace[((size_t)blockIdx.x * kTraceRoles + role) * (size_t)p.trace_cap + n] =
+            ((unsigned long long)ev << 56) | ((unsigned long long)(arg & 0xFFFFu) << 40) | (t & 0xFFFFFFFFFFull);
+        ++n;
+    }
+}
+#define FA_TRACE_DECL uint32_t tr_n = 0
+#define FA_TRACE_EV(cond, role, ev, arg) \
+    do {                                 \
+        if (cond) trace_event(p, role, tr_n, ev, arg); \
+    } while (0)
+#else
+#define FA_TRACE_DECL (void)0
+#define FA_TRACE_EV(cond, role, ev, arg) (void)0
+#endif
 
 // Wait-site codes recorded in the status word: role << 8 | barrier index.
 enum : uint32_t { kSiteSoftmax = 0x100, kSiteEpilogue = 0x300, kSiteLoad = 0x400, kSiteMma = 0x500,
@@ -155,11 +210,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
     const uint32_t tO = tmem + lane_base + C::col_o(t);
     const float sl2 = p.scale_log2;
     uint32_t ph_s = 0, ph_te = 0;
+    FA_TRACE_DECL;
+    const bool tr = (threadIdx.x & 127) == 0;
 
     for (int r = 0;; ++r) {
-        const int u = unit_at(r, p);
-        if (u < 0) break;
-        const Unit un = decode_unit(u, p);
+        Unit un;
+        const int ust = unit_at(r, p, un);
+        if (ust == kUnitDone) break;
+        if (ust == kUnitSkip) continue;
         const int nkv = un.nkv[t];
         if (nkv == 0) continue;
         float b = -INFINITY;   // base of the row, base-2 scaled units
@@ -167,13 +225,19 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
         for (int j = 0; j < nkv; ++j) {
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + t), ph_s, kSiteSoftmax | (kBarSFull + t))) return;
             ph_s ^= 1u;
+            FA_TRACE_EV(tr, t, kEvSReady, j);
             ptx::tc_fence_after();
+            // scores of the row; each 32-column load also returns its maximum
             uint32_t sr[128];
+            float pm[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sr + 32 * c);
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32_max(tS + 32 * c, sr + 32 * c, pm[c]);
             ptx::tmem_wait_ld();
             ptx::reg_fence(sr);
+            ptx::reg_fence(pm);
+            FA_TRACE_EV(tr, t, kEvSLoaded, j);
             float* s = reinterpret_cast<float*>(sr);
+            float mraw;
             if (p.mask_last && j == nkv - 1) {
                 // keys beyond the sequence, and (causal) keys after this row
                 const int qrow = un.q_tile[t] * kBM + row;
@@ -181,54 +245,73 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 if (p.causal) lim = min(lim, qrow - j * kBN);
 #pragma unroll
                 for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
-            }
-            float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+                // maximum over what is left: four chains of three-input max
+                float m[4];
 #pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-                m0 = fmaxf(m0, s[c]);
-                m1 = fmaxf(m1, s[c + 1]);
-                m2 = fmaxf(m2, s[c + 2]);
-                m3 = fmaxf(m3, s[c + 3]);
+                for (int k = 0; k < 4; ++k) m[k] = ptx::max3(s[32 * k], s[32 * k + 1], s[32 * k + 2]);
+#pragma unroll
+                for (int i = 3; i < 31; i += 2) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) m[k] = ptx::max3(m[k], s[32 * k + i], s[32 * k + i + 1]);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], s[32 * k + 31]);
+                mraw = fmaxf(ptx::max3(m[0], m[1], m[2]), m[3]);
+            } else {
+                mraw = fmaxf(ptx::max3(pm[0], pm[1], pm[2]), pm[3]);
             }
-            const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
+            const float mx = mraw * sl2;
             // conditional re-base: keep b unless the maximum passed b + 8
-            float hist = 1.f;
+            float h = 1.f;
             const float cand = fmaxf(b, mx);
             if (cand > b + kRebaseThreshold) {
-                hist = ptx::ex2(b - cand);   // 0 on the first tile (b = -inf)
+                h = ptx::ex2(b - cand);   // 0 on the first tile (b = -inf)
                 b = cand;
             }
-            if (j > 0 && __any_sync(0xffffffffu, hist < 1.f)) {
-                // rare path: scale this warp's 32 rows of O_t (PV_t(j-1) is complete)
+            FA_TRACE_EV(tr, t, kEvMaxDone, j);
+            if (j > 0 && __any_sync(0xffffffffu, h < 1.f)) {
+                // rare path: this warp's 32 rows of O_t are scaled by 2^(b_old - b_new)
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
                     ptx::tmem_ld32_wait(tO + c0, o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * hist);
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * h);
                     ptx::tmem_st32(tO + c0, o);
                 }
+                FA_TRACE_EV(tr, t, kEvRescale, j);
             }
+            // p = 2^(s * scale*log2e - b): one packed FMA per pair, two ex2,
+            // packed row sums in four independent accumulators; P is published
+            // in two halves of 64 keys
             const float nb = (b == -INFINITY) ? 0.f : -b;
-            float sum0 = 0.f, sum1 = 0.f;
+            const uint64_t c2 = ptx::f2_pack(sl2, sl2), nb2 = ptx::f2_pack(nb, nb);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ptx::ex2(fmaf(s[c * 32 + 2 * i], sl2, nb));
-                    const float p1 = ptx::ex2(fmaf(s[c * 32 + 2 * i + 1], sl2, nb));
-                    sum0 += p0;
-                    sum1 += p1;
+                    float x0, x1;
+                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nb2), x0, x1);
+                    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                    acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
                     pk[i] = ptx::pack2<kBF16>(p0, p1);
                 }
                 ptx::tmem_st16(tS + c * 16, pk);
+                if (c == 1 || c == 3) {
+                    // publish P (and, at c == 1, the rescaled O) for the MMA issuer
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bars + 8 * (c == 1 ? kBarPHalf + t : kBarPFull + t));
+                    if (c == 1) FA_TRACE_EV(tr, t, kEvExpDone, j);
+                }
             }
-            ptx::tmem_wait_st();
-            l = l * hist + (sum0 + sum1);
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarPFull + t));
+            FA_TRACE_EV(tr, t, kEvPDone, j);
+            float sa, sb;
+            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), sa, sb);
+            l = fmaf(l, h, sa + sb);
         }
         // hand (l, b) of every row to the epilogue
         if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarStEmpty + t), ph_te ^ 1u, kSiteSoftmax | (kBarStEmpty + t)))
@@ -241,11 +324,12 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
 }
 
 // ---------------------------------------------------------------------------------
-// Correction/epilogue warpgroup: O_t / l, LSE, convert, stage, TMA store.
+// Correction/epilogue warpgroup: per unit and query tile, the final correction
+// O_t / l, the LSE, conversion to 16 bits, shared-memory staging, TMA store.
 template <int D, bool kBF16>
-__device__ __forceinline__ void epilogue_role(const Params& p, const ptx::WaitCtx& wc, const CUtensorMap* tm_o,
-                                              uint32_t tmem, uint32_t smem_base, uint32_t bars, const float2* stats,
-                                              volatile uint32_t* ctl_go)
+__device__ __forceinline__ void correction_epilogue_role(const Params& p, const ptx::WaitCtx& wc,
+                                                         const CUtensorMap* tm_o, uint32_t tmem, uint32_t smem_base,
+                                                         uint32_t bars, const float2* stats, volatile uint32_t* ctl_go)
 {
     using C = Cfg<D>;
     const int lane = threadIdx.x & 31;
@@ -256,16 +340,18 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const ptx::WaitCt
     const uint32_t stage = smem_base + C::kOffStage;
     volatile uint32_t* go = ctl_go;   // leader's wait outcome, read by all 128 threads
     uint32_t ph_o = 0u, ph_t = 0u;   // phase bit of tile t at bit t
+    FA_TRACE_DECL;
 
     for (int r = 0;; ++r) {
-        const int u = unit_at(r, p);
-        if (u < 0) break;
-        const Unit un = decode_unit(u, p);
+        Unit un;
+        const int ust = unit_at(r, p, un);
+        if (ust == kUnitDone) break;
+        if (ust == kUnitSkip) continue;
+        // one named barrier carries the leader's wait outcome to all 128
+        // threads, so the warpgroup never splits over an abort
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (un.nkv[t] == 0) continue;
-            // the leader waits; one named barrier hands every thread the same
-            // outcome, so the warpgroup never splits over an abort
             if (leader) {
                 const bool ok = ptx::mbar_wait(wc, bars + 8 * (kBarOFull + t), (ph_o >> t) & 1u,
                                                kSiteEpilogue | (kBarOFull + t)) &&
@@ -277,6 +363,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const ptx::WaitCt
             if (go[0] == 0u) goto done;
             ph_o ^= 1u << t;
             ph_t ^= 1u << t;
+            FA_TRACE_EV(leader, kTrEpilogue, kEvOFull, t);
             ptx::tc_fence_after();
             const float2 st = stats[t * kBM + row];
             __syncwarp();
@@ -295,10 +382,14 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const ptx::WaitCt
                     uint32_t o[32];
                     ptx::tmem_ld32_wait(tO + box * 64 + half * 32, o);
                     uint32_t pk[16];
+                    const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[i] = ptx::pack2<kBF16>(__uint_as_float(o[2 * i]) * inv_l,
-                                                  __uint_as_float(o[2 * i + 1]) * inv_l);
+                    for (int i = 0; i < 16; ++i) {
+                        float a, b2;
+                        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
+                                       a, b2);
+                        pk[i] = ptx::pack2<kBF16>(a, b2);
+                    }
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         const int chunk = half * 4 + cc;   // 16-byte chunk of the 128-byte row
@@ -318,6 +409,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const ptx::WaitCt
                     ptx::bulk_commit();
                 }
             }
+            FA_TRACE_EV(leader, kTrEpilogue, kEvEpiDone, t);
         }
     }
 done:
@@ -336,10 +428,12 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
     uint32_t q_issued = 0u;    // bit t: a Q load into buffer t was issued
     uint32_t kv_count = 0;
     bool ok = true;
+    FA_TRACE_DECL;
     for (int r = 0; ok; ++r) {
-        const int u = unit_at(r, p);
-        if (u < 0) break;
-        const Unit un = decode_unit(u, p);
+        Unit un;
+        const int ust = unit_at(r, p, un);
+        if (ust == kUnitDone) break;
+        if (ust == kUnitSkip) continue;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (!ok || un.nkv[t] == 0) continue;
@@ -355,6 +449,7 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
             for (int bx = 0; bx < C::kBoxes; ++bx)
                 ptx::tma_load_3d(tm_q, dst + bx * C::kBoxBytes, fb, bx * 64, un.q_tile[t] * kBM, un.bh);
             q_issued |= 1u << t;
+            FA_TRACE_EV(true, kTrLoad, kEvQLoad, t);
         }
         for (int j = 0; j < un.nmax && ok; ++j) {
 #pragma unroll 1
@@ -375,6 +470,7 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
 #pragma unroll
                 for (int bx = 0; bx < C::kBoxes; ++bx)
                     ptx::tma_load_3d(m, dst + bx * C::kBoxBytes, fb, bx * 64, j * kBN, un.bh);
+                FA_TRACE_EV(true, kTrLoad, kEvKVLoad, idx);
             }
         }
     }
@@ -398,8 +494,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);   // Q, K both K-major
     constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, kBF16, true);      // V is MN-major (D contiguous)
-    uint32_t ph_q = 0u, ph_p = 0u, ph_oe = 0u;   // phase bit of tile t at bit t
+    uint32_t ph_q = 0u, ph_ph = 0u, ph_p = 0u, ph_oe = 0u;   // phase bit of tile t at bit t
     uint32_t kv_count = 0;
+    FA_TRACE_DECL;
 
     auto kv_wait = [&](uint32_t idx) -> bool {
         const uint32_t slot = idx % C::kSlots;
@@ -422,20 +519,25 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     // O_t += P_t V: A = P from TMEM (16 keys = 8 columns per step), B = V tile
     // [128 keys x D], D contiguous: 8-key groups 1024 bytes apart, 64-column
     // boxes kBoxBytes apart.
-    auto issue_pv = [&](int t, uint32_t idx, bool acc) {
+    // One half: keys 64*half .. 64*half+63 (four K=16 steps).
+    auto issue_pv = [&](int t, uint32_t idx, int half, bool acc) {
         const uint32_t vb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = half * 4 + k4;
             ptx::mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
                         ptx::sdesc_sw128(vb + kk * 16 * 128, C::kBoxBytes, 1024), kIdescPV,
                         (acc || kk > 0) ? 1u : 0u);
+        }
     };
 
     for (int r = 0;; ++r) {
-        const int u = unit_at(r, p);
-        if (u < 0) break;
-        const Unit un = decode_unit(u, p);
+        Unit un;
+        const int ust = unit_at(r, p, un);
+        if (ust == kUnitDone) break;
+        if (ust == kUnitSkip) continue;
         const uint32_t kvb = kv_count;   // K_j is entry kvb + 2j of the ring, V_j is kvb + 2j + 1
+        FA_TRACE_EV(true, kTrMma, kEvUnit, un.id);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (un.nkv[t] == 0) continue;
@@ -449,6 +551,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             if (un.nkv[t] == 0) continue;
             issue_qk(t, kvb);
             ptx::mma_commit(bars + 8 * (kBarSFull + t));
+            FA_TRACE_EV(true, kTrMma, kEvQK, (uint32_t)t << 12);
             if (un.nkv[t] == 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
         }
         kv_release(kvb);
@@ -458,9 +561,10 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (j < un.nkv[t]) {
-                    if (!ptx::mbar_wait(wc, bars + 8 * (kBarPFull + t), (ph_p >> t) & 1u, kSiteMma | (kBarPFull + t)))
+                    FA_TRACE_EV(true, kTrMma, kEvPWait, ((uint32_t)t << 12) | j);
+                    if (!ptx::mbar_wait(wc, bars + 8 * (kBarPHalf + t), (ph_ph >> t) & 1u, kSiteMma | (kBarPHalf + t)))
                         goto done;
-                    ph_p ^= 1u << t;
+                    ph_ph ^= 1u << t;
                     if (j == 0) {
                         // O_t is overwritten: the previous unit's epilogue must have read it
                         if (!ptx::mbar_wait(wc, bars + 8 * (kBarOEmpty + t), ((ph_oe >> t) & 1u) ^ 1u,
@@ -473,7 +577,13 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                         v_ready = true;
                     }
                     ptx::tc_fence_after();
-                    issue_pv(t, iv, j > 0);
+                    issue_pv(t, iv, 0, j > 0);
+                    if (!ptx::mbar_wait(wc, bars + 8 * (kBarPFull + t), (ph_p >> t) & 1u, kSiteMma | (kBarPFull + t)))
+                        goto done;
+                    ph_p ^= 1u << t;
+                    ptx::tc_fence_after();
+                    issue_pv(t, iv, 1, true);
+                    FA_TRACE_EV(true, kTrMma, kEvPV, ((uint32_t)t << 12) | j);
                     if (j == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarOFull + t));
                 }
                 if (j + 1 < un.nkv[t]) {
@@ -484,6 +594,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     }
                     issue_qk(t, ik);
                     ptx::mma_commit(bars + 8 * (kBarSFull + t));
+                    FA_TRACE_EV(true, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
                     if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
                 }
             }
@@ -521,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars + 8 * (kBarQFull + t), 1);
             ptx::mbar_init(bars + 8 * (kBarQEmpty + t), 1);
             ptx::mbar_init(bars + 8 * (kBarSFull + t), 1);
+            ptx::mbar_init(bars + 8 * (kBarPHalf + t), 4);
             ptx::mbar_init(bars + 8 * (kBarPFull + t), 4);
             ptx::mbar_init(bars + 8 * (kBarOFull + t), 1);
             ptx::mbar_init(bars + 8 * (kBarOEmpty + t), 4);
@@ -552,13 +664,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const ptx::WaitCtx wc{base + C::kOffCtl + 4, p.timeout_ns, p.status};
 
     if (warp < 8) {
-        ptx::setmaxnreg_inc<kRegSoftmax>();
+        ptx::setmaxnreg_inc<RegSplit<D>::kSoftmax>();
         softmax_role<D, kBF16>(p, wc, warp >> 2, tmem, bars, stats);
     } else if (warp < 12) {
-        ptx::setmaxnreg_dec<kRegEpilogue>();
-        epilogue_role<D, kBF16>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
+        ptx::setmaxnreg_dec<RegSplit<D>::kEpilogue>();
+        correction_epilogue_role<D, kBF16>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
     } else {
-        ptx::setmaxnreg_dec<kRegControl>();
+        ptx::setmaxnreg_dec<RegSplit<D>::kControl>();
         if (warp == 12) {
             if (lane == 0) load_role<D>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {

@@ -310,6 +310,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r)
         : "memory");
 }
 
+// Load 32 columns without waiting and, in the same instruction, reduce them to
+// their maximum (per thread = per TMEM lane): the row maximum of a 32-column
+// slice comes with the load.
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t* r, float& mx)
+{
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+        : FA_R8(0), FA_R8(8), FA_R8(16), FA_R8(24), "=f"(mx)
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Compiler-level fence: every use of r[] depends on a (volatile, hence ordered)
@@ -319,6 +333,13 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N])
 {
 #pragma unroll
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+template <int N>
+__device__ __forceinline__ void reg_fence(float (&r)[N])
+{
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+f"(r[i]));
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
@@ -359,6 +380,49 @@ __device__ __forceinline__ float lg2(float x)
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// ---- packed fp32 pairs (one instruction, two lanes of work) -------------------
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// max of three fp32 values in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 // Two fp32 values -> one 32-bit word of two 16-bit values, round to nearest

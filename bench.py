@@ -47,6 +47,43 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def source_hash() -> str:
+    """sha256 over the CUDA sources and the C header: identifies the kernel build."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "attention_fa_fwd_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "fa_fwd.h"))
+    for fn in files:
+        h.update(os.path.basename(fn).encode())
+        with open(fn, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload, or
+    None when there is none or it was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.md")
+    try:
+        with open(path, encoding="utf-8") as f:
+            text = f.read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        line = line.strip().strip("`")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_sha256") != source_hash():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -276,7 +313,15 @@ def run_ours(args, w):
         return 0
 
     pk, pk_kind = peaks()
-    peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # a loop timed for half a second or more runs at the power-capped clock:
+    # compare it with the sustained GEMM peak, a short burst with the burst peak
+    if ms_max >= 500.0:
+        peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        peak_kind = f"bf16 dense sustained ({pk_kind})"
+    else:
+        peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        peak_kind = f"bf16 dense burst ({pk_kind})"
+    traffic = args.traffic if args.traffic is not None else profiled_traffic(w.name)
     achieved = flops / (ms_step * 1e-3) / 1e12   # one launch per step on this stream
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
@@ -291,7 +336,7 @@ def run_ours(args, w):
                    "units": info["units"]},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "peak_kind": f"bf16 dense burst ({pk_kind})", "traffic": args.traffic},
+                     "peak_kind": peak_kind, "timed_ms": round(ms_max, 1), "traffic": traffic},
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * world,

@@ -98,8 +98,9 @@ typedef struct {
     int smem_bytes;      /* dynamic shared memory per CTA */
     int tiles_per_unit;  /* 128-row query tiles per work unit (1 or 2) */
     int units;           /* work units = B*H * ceil(query tiles / tiles_per_unit) */
-    int head_group;      /* heads scheduled together (longest units first within a group) */
+    int head_group;      /* snake schedule: heads scheduled together (longest units first) */
     int num_sms;         /* SM count of the current device */
+    int schedule;        /* 0 = snake over units, 1 = causal mirror pairs (see the kernel source) */
 } fa_launch_info_t;
 
 /*
