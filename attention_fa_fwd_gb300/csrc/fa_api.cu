@@ -176,13 +176,23 @@ void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t*
     const int n_qgroups = (n_qtiles + tpu - 1) / tpu;
     const long long units = (long long)BH * n_qgroups;
     const int grid = (int)(units < num_sms ? units : num_sms);
-    // Causal units differ in cost.  With more than one round of units, pair
-    // each query group with its mirror (equal cost per pair, and the pair shares
-    // its head's K/V in L2); with a single round every CTA takes one unit.
-    // Without the mask every unit costs the same and heads simply go in order.
-    const bool pairs = causal && units > grid;
-    const int head_group =
-        (causal && !pairs) ? plan_head_group(BH, S, D, n_qtiles, tpu, n_qgroups, units, grid) : 1;
+    // Causal units differ in cost.  The snake over head groups balances best
+    // (the planner replays it), but each of its rounds holds about
+    // grid / head_group units of a head; with fewer than four, CTAs rarely share
+    // a head's K/V in L2 and the re-reads go to DRAM (4x32x4096x128 bf16: 1.1 GB
+    // per launch against 0.4 GB, and under a one-second loop the GPU hits its
+    // power cap).  Then the mirror-pair schedule is used instead: slightly worse
+    // balance, but a CTA's two units share one head and a round covers few heads.
+    // With a single round every CTA takes one unit.  Without the mask every unit
+    // costs the same and heads simply go in order.
+    int head_group = 1;
+    bool pairs = false;
+    if (causal && units > grid) {
+        head_group = plan_head_group(BH, S, D, n_qtiles, tpu, n_qgroups, units, grid);
+        pairs = grid < 4 * head_group;
+    } else if (causal) {
+        head_group = plan_head_group(BH, S, D, n_qtiles, tpu, n_qgroups, units, grid);
+    }
     const int pairs_per_head = (n_qgroups + 1) / 2;
     if (info) {
         info->grid = grid;
