@@ -199,6 +199,16 @@ def time_oracle(w, q, k, v, budget_s: float, steps: int, seed: int = 0):
     return statistics.median(tflops), statistics.median(per_step), desc, nthreads
 
 
+def aggregate(ms_local: float, flops_per_rank: float, world: int, dist=None, device=None):
+    """Max of the ranks' timed milliseconds and the whole-job TFLOPS over it
+    (every rank ran `flops_per_rank`).  `dist` is torch.distributed or None."""
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if dist is not None and world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, flops_per_rank * world / (ms_max * 1e-3) / 1e12
+
+
 def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -271,13 +281,9 @@ def run_ours(args, w):
     status, site = fa.device_status(clear=True, stream=stream)
     if status != fa.FA_OK:
         raise SystemExit(f"in-kernel wait gave up at site {site:#x}")
-    t = torch.tensor([ms], device=dev, dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    ms_step = ms_max / args.steps
     flops = w.flops()
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    ms_max, value = aggregate(ms, flops * args.steps, world, dist, dev)
+    ms_step = ms_max / args.steps
 
     # end to end through the C ABI with host buffers: H2D of q, k, v, the
     # kernel, D2H of o and lse, every step
@@ -300,10 +306,7 @@ def run_ours(args, w):
         e2e_step()
     e1.record(stream)
     barrier()
-    te = torch.tensor([e0.elapsed_time(e1) / e2e_steps], device=dev, dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = flops * world / (float(te.item()) * 1e-3) / 1e12
+    _, e2e_value = aggregate(e0.elapsed_time(e1) / e2e_steps, flops, world, dist, dev)
     h2d = 3 * q.numel() * q.element_size()
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
 
