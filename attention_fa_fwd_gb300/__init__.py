@@ -19,7 +19,7 @@ import torch
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_hostio", "launch_info", "plan", "device_status",
+__all__ = ["fa_fwd", "fa_fwd_splitkv", "splitkv_workspace_bytes", "fa_fwd_hostio", "launch_info", "plan", "device_status",
            "selftest_wait_timeout", "strerror", "build", "lib", "header_functions",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FaError"]
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         dims = [i, i, i, i, i, f, i, vp]
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp] + dims
         L.fa_fwd_hostio.argtypes = [vp] * 10 + dims
+        L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
+        L.fa_fwd_splitkv_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         L.fa_fwd_launch_info.argtypes = [i, i, i, i, i, i, ctypes.POINTER(LaunchInfo)]
         L.fa_fwd_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(LaunchInfo)]
         L.fa_device_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint)]
@@ -69,7 +71,8 @@ def lib() -> ctypes.CDLL:
         L.fa_strerror.argtypes = [i]
         L.fa_strerror.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_fwd_hostio", "fa_fwd_launch_info", "fa_fwd_plan",
-                     "fa_device_status", "fa_selftest_wait_timeout"):
+                     "fa_device_status", "fa_selftest_wait_timeout", "fa_fwd_splitkv",
+                     "fa_fwd_splitkv_workspace"):
             getattr(L, name).restype = i
         _lib = L
     return _lib
@@ -79,7 +82,7 @@ def header_functions() -> list[str]:
     """Names of the functions include/fa_fwd.h declares."""
     with open(HEADER, encoding="utf-8") as fh:
         text = fh.read()
-    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^(?:int|const char\*|size_t)\s+(fa_\w+)\s*\(", text, re.M)))
 
 
 def strerror(status: int) -> str:
@@ -134,6 +137,46 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
                           _stream_ptr(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+    return out, lse
+
+
+def splitkv_workspace_bytes(B: int, H: int, S: int, D: int, causal: bool,
+                            dtype=torch.bfloat16) -> int:
+    """Workspace bytes fa_fwd_splitkv needs on the current device (0: no split)."""
+    n = ctypes.c_size_t(0)
+    rc = lib().fa_fwd_splitkv_workspace(B, H, S, D, int(bool(causal)), _DTYPE.get(dtype, 99),
+                                        ctypes.byref(n))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv_workspace")
+    return n.value
+
+
+def fa_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                   scale: float | None = None, workspace: torch.Tensor | None = None,
+                   out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """fa_fwd for problems too small to fill the GPU in one pass: key ranges are
+    split into chunks whose partial results are merged by a second kernel.
+    `workspace` (a CUDA byte tensor) defaults to a fresh torch allocation of
+    the size splitkv_workspace_bytes reports."""
+    _check_qkv(q, k, v)
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        need = splitkv_workspace_bytes(B, H, S, D, causal, q.dtype)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        ws_bytes = workspace.numel() * workspace.element_size()
+        rc = lib().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr(), B, H, S, D, int(bool(causal)), float(scale),
+                                  _DTYPE[q.dtype], workspace.data_ptr(), ws_bytes,
+                                  _stream_ptr(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv")
     return out, lse
 
 

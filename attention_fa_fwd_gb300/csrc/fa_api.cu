@@ -218,7 +218,51 @@ void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t*
         p->n_pairs = (long long)BH * pairs_per_head;
         p->causal = causal;
         p->mask_last = (causal || (S % fa::kBN) != 0) ? 1 : 0;
+        p->split_chunk = 0;
+        p->units_per_head = 0;
+        p->ws_o = nullptr;
+        p->ws_lse = nullptr;
     }
+}
+
+// ---- split-KV planner ---------------------------------------------------------
+// When one pass has fewer work units than SMs (few heads, short rows), the key
+// range of every query group is cut into chunks of `chunk` key tiles, each a
+// unit of its own; the largest chunk that still gives every SM a unit is used.
+// Returns false when one pass already fills the GPU or no split would help.
+struct SplitPlan {
+    int chunk, tpu, n_qtiles, n_qgroups, units_per_head;
+    long long units;
+};
+
+bool plan_split(int BH, int S, int causal, int num_sms, SplitPlan* sp)
+{
+    const int n_qtiles = (S + kBM - 1) / kBM;
+    const int tpu1 = ((long long)BH * n_qtiles >= 2ll * num_sms) ? 2 : 1;
+    const long long units1 = (long long)BH * ((n_qtiles + tpu1 - 1) / tpu1);
+    if (units1 >= num_sms) return false;
+    const int tpu = n_qtiles >= 2 ? 2 : 1;
+    const int n_qgroups = (n_qtiles + tpu - 1) / tpu;
+    int chunk = 1, uph = 0;
+    for (int c = n_qtiles; c >= 1; --c) {
+        uph = 0;
+        for (int g = 0; g < n_qgroups; ++g) uph += fa::split_chunks(g, tpu, n_qtiles, n_qtiles, causal, c);
+        chunk = c;
+        if ((long long)BH * uph >= num_sms) break;
+    }
+    if (chunk >= n_qtiles) return false;   // every group would be one chunk: nothing to gain
+    sp->chunk = chunk;
+    sp->tpu = tpu;
+    sp->n_qtiles = n_qtiles;
+    sp->n_qgroups = n_qgroups;
+    sp->units_per_head = uph;
+    sp->units = (long long)BH * uph;
+    return true;
+}
+
+size_t split_workspace_bytes(const SplitPlan& sp, int D)
+{
+    return (size_t)sp.units * sp.tpu * kBM * (size_t)(D + 1) * sizeof(float);
 }
 
 // [B*H, S, D] 16-bit tensor, 128-row x 64-column boxes, 128-byte swizzle.
@@ -279,8 +323,13 @@ int fa_fwd_plan(int B, int H, int S, int D, int causal, int dtype, int num_sms, 
     return FA_OK;
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D, int causal,
-           float scale, int dtype, void* stream)
+}  // extern "C"
+
+namespace {
+
+// Common checks of the forward entry points; fills the SM count.
+int check_call(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H, int S,
+               int D, int causal, float scale, int dtype, int* num_sms)
 {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
@@ -288,16 +337,34 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     if (rc != FA_OK) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_MISALIGNED;
-    int num_sms = 0, cc = 0;
-    rc = device_props(&num_sms, &cc);
+    int cc = 0;
+    rc = device_props(num_sms, &cc);
     if (rc != FA_OK) return rc;
     if (cc != 103) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
 
+// One attention launch (and, with a split plan, the merge launch after it).
+int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D, int causal,
+            float scale, int dtype, int num_sms, const SplitPlan* sp, float* ws, void* stream)
+{
     fa::LaunchArgs a;
     plan(B, H, S, D, causal, num_sms, nullptr, &a.p);
     fa_launch_info_t info;
     plan(B, H, S, D, causal, num_sms, &info, nullptr);
     a.grid = info.grid;
+    const int BH = B * H;
+    if (sp) {
+        a.p.tpu = sp->tpu;
+        a.p.n_qgroups = sp->n_qgroups;
+        a.p.n_units = (int)sp->units;
+        a.p.split_chunk = sp->chunk;
+        a.p.units_per_head = sp->units_per_head;
+        a.p.sched = fa::kSchedSnake;
+        a.p.ws_o = ws;
+        a.p.ws_lse = ws + (size_t)sp->units * sp->tpu * kBM * D;
+        a.grid = (int)(sp->units < num_sms ? sp->units : num_sms);
+    }
     a.p.lse = lse;
     a.p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.p.timeout_ns = timeout_ns();
@@ -312,7 +379,6 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     void* status = nullptr;
     if (cudaGetSymbolAddress(&status, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
     a.p.status = static_cast<unsigned int*>(status);
-    const int BH = B * H;
     if (make_tmap(&a.tm_q, q, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_k, k, BH, S, D, dtype) != FA_OK ||
         make_tmap(&a.tm_v, v, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_o, o, BH, S, D, dtype) != FA_OK)
         return FA_ERR_CUDA;
@@ -323,7 +389,67 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         e = dtype == FA_DTYPE_BF16 ? fa::launch_d64_bf16(a, s) : fa::launch_d64_f16(a, s);
     else
         e = dtype == FA_DTYPE_BF16 ? fa::launch_d128_bf16(a, s) : fa::launch_d128_f16(a, s);
-    return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    if (e != (int)cudaSuccess) return FA_ERR_CUDA;
+    if (sp) {
+        fa::MergeArgs m;
+        m.ws_o = a.p.ws_o;
+        m.ws_lse = a.p.ws_lse;
+        m.o = o;
+        m.lse = lse;
+        m.BH = BH;
+        m.S = S;
+        m.D = D;
+        m.n_qtiles = sp->n_qtiles;
+        m.n_kv = sp->n_qtiles;
+        m.tpu = sp->tpu;
+        m.causal = causal;
+        m.chunk = sp->chunk;
+        m.units_per_head = sp->units_per_head;
+        m.bf16 = dtype == FA_DTYPE_BF16;
+        if (fa::launch_merge(m, s) != (int)cudaSuccess) return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D, int causal,
+           float scale, int dtype, void* stream)
+{
+    int num_sms = 0;
+    const int rc = check_call(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, &num_sms);
+    if (rc != FA_OK) return rc;
+    return run_fwd(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, num_sms, nullptr, nullptr, stream);
+}
+
+int fa_fwd_splitkv_workspace(int B, int H, int S, int D, int causal, int dtype, size_t* bytes)
+{
+    if (!bytes) return FA_ERR_INVALID_ARG;
+    int rc = check_args(B, H, S, D, causal, dtype);
+    if (rc != FA_OK) return rc;
+    int num_sms = 0, cc = 0;
+    rc = device_props(&num_sms, &cc);
+    if (rc != FA_OK) return rc;
+    SplitPlan sp;
+    *bytes = plan_split(B * H, S, causal, num_sms, &sp) ? split_workspace_bytes(sp, D) : 0;
+    return FA_OK;
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D,
+                   int causal, float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream)
+{
+    int num_sms = 0;
+    const int rc = check_call(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, &num_sms);
+    if (rc != FA_OK) return rc;
+    SplitPlan sp;
+    if (!plan_split(B * H, S, causal, num_sms, &sp))
+        return run_fwd(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, num_sms, nullptr, nullptr, stream);
+    if (!workspace || workspace_bytes < split_workspace_bytes(sp, D)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return FA_ERR_MISALIGNED;
+    return run_fwd(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, num_sms, &sp, static_cast<float*>(workspace),
+                   stream);
 }
 
 int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, void* q_d, void* k_d,
@@ -377,7 +503,7 @@ int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream)
 
 #ifdef FA_TRACE
 // Trace build only: every later fa_fwd records events of CTAs [0, ctas) into
-// `buf` (device, ctas * 5 * cap 64-bit words, caller-owned, zeroed by the caller).
+// `buf` (device, ctas * 6 * cap 64-bit words, caller-owned, zeroed by the caller).
 int fa_trace_set(unsigned long long* buf, int ctas, int cap)
 {
     if ((buf == nullptr) != (ctas == 0) || ctas < 0 || cap < 0) return FA_ERR_INVALID_ARG;

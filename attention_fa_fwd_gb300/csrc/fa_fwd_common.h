@@ -30,6 +30,14 @@ struct Params {
     int causal;                 // 1: key j allowed for query i iff j <= i
     int mask_last;              // the last K/V tile of a query tile needs masking
     float scale_log2;           // scale * log2(e)
+    // Split-KV mode (split_chunk > 0): a unit covers key tiles
+    // [chunk * split_chunk, (chunk + 1) * split_chunk) of one query group and
+    // writes its O (normalised by its own row sums, fp32) and LSE to the
+    // workspace; fa_merge combines the chunks of each row.
+    int split_chunk;            // key tiles per chunk, 0 = no split
+    int units_per_head;         // split: sum over query groups of their chunk counts
+    float* ws_o;                // split: [n_units][tpu][128][D] fp32
+    float* ws_lse;              // split: [n_units][tpu][128] fp32
     // Event trace (used only by the FA_TRACE build): per traced CTA and role,
     // `trace_cap` 64-bit records of event, argument and SM clock.
     unsigned long long* trace;
@@ -39,7 +47,8 @@ struct Params {
 
 // Trace roles and events (FA_TRACE build).  A record is
 // event << 56 | (arg & 0xFFFF) << 40 | (clock64 & (2^40 - 1)).
-enum TraceRole : int { kTrSoftmax0 = 0, kTrSoftmax1 = 1, kTrEpilogue = 2, kTrLoad = 3, kTrMma = 4, kTraceRoles = 5 };
+enum TraceRole : int { kTrSoftmax0 = 0, kTrSoftmax1 = 1, kTrEpilogue = 2, kTrLoad = 3, kTrMma = 4, kTrKernel = 5,
+                       kTraceRoles = 6 };
 enum TraceEvent : unsigned {
     kEvSReady = 1,      // softmax: scores of key tile j visible (arg j)
     kEvPDone = 2,       // softmax: P of key tile j published (arg j)
@@ -51,13 +60,43 @@ enum TraceEvent : unsigned {
     kEvQK = 11,         // MMA: QK issued (arg t << 12 | j)
     kEvPV = 12,         // MMA: PV issued (arg t << 12 | j)
     kEvPWait = 13,      // MMA: starts waiting for P (arg t << 12 | j)
+    kEvPVGo = 14,       // MMA: first half of P ready, first PV half about to issue (arg t << 12 | j)
+    kEvPVMid = 15,      // MMA: first PV half issued (arg t << 12 | j)
+    kEvQKGo = 16,       // MMA: about to issue QK (arg t << 12 | j)
     kEvQLoad = 20,      // load: Q tile issued (arg t)
     kEvKVLoad = 21,     // load: K or V tile issued (arg ring index)
     kEvOFull = 30,      // epilogue: O of tile t complete (arg t)
     kEvEpiDone = 31,    // epilogue: tile t stored (arg t)
+    kEvEntry = 40,      // kernel: thread 0 entered
+    kEvSetup = 41,      // kernel: barriers initialised, TMEM allocated
+    kEvExit = 42,       // kernel: all roles done, before TMEM is freed
 };
 
 enum : int { kSchedSnake = 0, kSchedPairs = 1 };
+
+// Key tiles a query tile visits: all of them, or up to its diagonal when causal.
+__host__ __device__ inline int kv_tiles_of(int q_tile, int n_kv, int causal)
+{
+    return causal ? (q_tile + 1 < n_kv ? q_tile + 1 : n_kv) : n_kv;
+}
+
+// Split-KV: number of key chunks of query group qg (its last tile sets the range).
+__host__ __device__ inline int split_chunks(int qg, int tpu, int n_qtiles, int n_kv, int causal, int chunk)
+{
+    int last_tile = qg * tpu + tpu - 1;
+    if (last_tile > n_qtiles - 1) last_tile = n_qtiles - 1;
+    return (kv_tiles_of(last_tile, n_kv, causal) + chunk - 1) / chunk;
+}
+
+// Split-KV merge: combine the chunk partials of every row into O (dtype) and LSE.
+struct MergeArgs {
+    const float* ws_o;
+    const float* ws_lse;
+    void* o;
+    float* lse;
+    int BH, S, D, n_qtiles, n_kv, tpu, causal, chunk, units_per_head, bf16;
+};
+int launch_merge(const MergeArgs& a, cudaStream_t s);
 
 struct LaunchArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;
@@ -71,6 +110,10 @@ int launch_d64_f16(const LaunchArgs& a, cudaStream_t s);
 int launch_d64_bf16(const LaunchArgs& a, cudaStream_t s);
 int launch_d128_f16(const LaunchArgs& a, cudaStream_t s);
 int launch_d128_bf16(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_f16_split(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_bf16_split(const LaunchArgs& a, cudaStream_t s);
+int launch_d128_f16_split(const LaunchArgs& a, cudaStream_t s);
+int launch_d128_bf16_split(const LaunchArgs& a, cudaStream_t s);
 
 // Dynamic shared memory of the instance for head dim D.
 int smem_bytes_for(int D);

@@ -63,11 +63,18 @@ constexpr float kLn2 = 0.693147180559945309f;
 // Register budget per warpgroup after setmaxnreg: softmax x2, epilogue, control
 // (load + MMA).  The four add up to 512 = 65536 registers / 128 threads; the
 // splits are the spill-free ones ptxas -v reports for each head dim.
-template <int D> struct RegSplit;
-template <> struct RegSplit<128> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 64, kControl = 96; };
-template <> struct RegSplit<64> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 72, kControl = 88; };
-static_assert(2 * RegSplit<128>::kSoftmax + RegSplit<128>::kEpilogue + RegSplit<128>::kControl == 512, "");
-static_assert(2 * RegSplit<64>::kSoftmax + RegSplit<64>::kEpilogue + RegSplit<64>::kControl == 512, "");
+template <int D, bool kSplit> struct RegSplit;
+template <> struct RegSplit<128, false> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 64, kControl = 96; };
+template <> struct RegSplit<64, false> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 72, kControl = 88; };
+template <> struct RegSplit<128, true> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 48, kControl = 96; };
+template <> struct RegSplit<64, true> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 48, kControl = 96; };
+template <int D, bool kSplit>
+constexpr bool reg_split_fits()
+{
+    return 2 * RegSplit<D, kSplit>::kSoftmax + RegSplit<D, kSplit>::kEpilogue + RegSplit<D, kSplit>::kControl == 512;
+}
+static_assert(reg_split_fits<128, false>() && reg_split_fits<64, false>(), "register split must add up to 512");
+static_assert(reg_split_fits<128, true>() && reg_split_fits<64, true>(), "register split must add up to 512");
 
 // Barrier indices inside the barrier array.
 enum : int {
@@ -107,11 +114,13 @@ struct Cfg {
 
 struct Unit {
     int status;      // kUnitDone, kUnitOk or kUnitSkip
-    int id;          // position of the unit in the schedule (trace only)
+    int id;          // position of the unit in the schedule (split: its workspace slot)
     int bh;
+    int j0;          // first key tile of the unit (0 unless split)
     int q_tile[2];   // query tile index of each tile of the unit
-    int nkv[2];      // key tiles to visit per tile (0 = tile absent)
-    int nmax;
+    int nkv[2];      // end (exclusive) of the key tiles tile t visits; 0 = tile absent
+    int last[2];     // the tile's last key tile overall: the one the mask applies to
+    int nmax;        // max of nkv
 };
 
 enum : int { kUnitDone = 0, kUnitOk = 1, kUnitSkip = 2 };
@@ -133,13 +142,31 @@ enum : int { kUnitDone = 0, kUnitOk = 1, kUnitSkip = 2 };
 // Returned by value: a unit the caller keeps by reference becomes
 // address-taken and its fields are reloaded from local memory in the MMA
 // issuer's inner loop (measured: 8% slower).
+template <bool kSplit>
 __device__ __forceinline__ Unit unit_at(int r, const Params& p)
 {
     const long long G = gridDim.x, c = blockIdx.x;
     Unit un;
     un.status = kUnitOk;
+    un.j0 = 0;
     int bh, qg;
-    if (p.sched == kSchedPairs) {
+    if constexpr (kSplit) {
+        // (head, query group, key chunk), dense and in that order
+        const long long u = (long long)r * G + c;
+        un.status = u >= p.n_units ? kUnitDone : kUnitOk;
+        const int ui = (int)u;
+        bh = ui / p.units_per_head;
+        int rem = ui - bh * p.units_per_head;
+        qg = 0;
+        for (int n = split_chunks(0, p.tpu, p.n_qtiles, p.n_kv, p.causal, p.split_chunk);
+             rem >= n && qg + 1 < p.n_qgroups;
+             n = split_chunks(qg, p.tpu, p.n_qtiles, p.n_kv, p.causal, p.split_chunk)) {
+            rem -= n;
+            ++qg;
+        }
+        un.j0 = rem * p.split_chunk;
+        un.id = ui;
+    } else if (p.sched == kSchedPairs) {
         // 32-bit arithmetic: pair indices stay below 2^31 (a 64-bit division
         // would bring in a called subroutine and slowed the whole kernel)
         const long long pl = (long long)(r >> 1) * G + c;
@@ -171,8 +198,15 @@ __device__ __forceinline__ Unit unit_at(int r, const Params& p)
     for (int t = 0; t < 2; ++t) {
         const int qt = qg * p.tpu + t;
         const bool active = (t < p.tpu) && (qt < p.n_qtiles);
+        const int total = kv_tiles_of(qt, p.n_kv, p.causal);
         un.q_tile[t] = qt;
-        un.nkv[t] = active ? (p.causal ? min(qt + 1, p.n_kv) : p.n_kv) : 0;
+        un.last[t] = total - 1;
+        if constexpr (kSplit) {
+            const int end = min(un.j0 + p.split_chunk, total);
+            un.nkv[t] = (active && end > un.j0) ? end : 0;
+        } else {
+            un.nkv[t] = active ? total : 0;
+        }
         un.nmax = max(un.nmax, un.nkv[t]);
     }
     return un;
@@ -206,7 +240,7 @@ enum : uint32_t { kSiteSoftmax = 0x100, kSiteEpilogue = 0x300, kSiteLoad = 0x400
 
 // ---------------------------------------------------------------------------------
 // Softmax warpgroup t: one thread per query row of tile t.
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kSplit>
 __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx& wc, int t, uint32_t tmem,
                                              uint32_t bars, float2* stats)
 {
@@ -223,16 +257,18 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
     const bool tr = (threadIdx.x & 127) == 0;
 
     for (int r = 0;; ++r) {
-        const Unit un = unit_at(r, p);
+        const Unit un = unit_at<kSplit>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         // t is a runtime value: select instead of indexing, so the unit stays in registers
         const int nkv = t ? un.nkv[1] : un.nkv[0];
         const int q_tile = t ? un.q_tile[1] : un.q_tile[0];
+        // the masked tile: the row's last key tile (always nkv - 1 without a split)
+        const int last = kSplit ? (t ? un.last[1] : un.last[0]) : nkv - 1;
         if (nkv == 0) continue;
         float b = -INFINITY;   // base of the row, base-2 scaled units
         float l = 0.f;         // running sum of 2^(x - b)
-        for (int j = 0; j < nkv; ++j) {
+        for (int j = un.j0; j < nkv; ++j) {
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + t), ph_s, kSiteSoftmax | (kBarSFull + t))) return;
             ph_s ^= 1u;
             FA_TRACE_EV(tr, t, kEvSReady, j);
@@ -248,7 +284,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             FA_TRACE_EV(tr, t, kEvSLoaded, j);
             float* s = reinterpret_cast<float*>(sr);
             float mraw;
-            if (p.mask_last && j == nkv - 1) {
+            if (p.mask_last && j == last) {
                 // keys beyond the sequence, and (causal) keys after this row
                 const int qrow = q_tile * kBM + row;
                 int lim = p.S - 1 - j * kBN;
@@ -279,7 +315,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 b = cand;
             }
             FA_TRACE_EV(tr, t, kEvMaxDone, j);
-            if (j > 0 && __any_sync(0xffffffffu, h < 1.f)) {
+            if (j > un.j0 && __any_sync(0xffffffffu, h < 1.f)) {
                 // rare path: this warp's 32 rows of O_t are scaled by 2^(b_old - b_new)
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
@@ -336,7 +372,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
 // ---------------------------------------------------------------------------------
 // Correction/epilogue warpgroup: per unit and query tile, the final correction
 // O_t / l, the LSE, conversion to 16 bits, shared-memory staging, TMA store.
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kSplit>
 __device__ __forceinline__ void correction_epilogue_role(const Params& p, const ptx::WaitCtx& wc,
                                                          const CUtensorMap* tm_o, uint32_t tmem, uint32_t smem_base,
                                                          uint32_t bars, const float2* stats, volatile uint32_t* ctl_go)
@@ -353,7 +389,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
     FA_TRACE_DECL;
 
     for (int r = 0;; ++r) {
-        const Unit un = unit_at(r, p);
+        const Unit un = unit_at<kSplit>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         // one named barrier carries the leader's wait outcome to all 128
@@ -378,8 +414,32 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarStEmpty + t));
             const float inv_l = 1.0f / st.x;
+            const float row_lse = (st.y + ptx::lg2(st.x)) * kLn2;
+            if constexpr (kSplit) {
+                // split-KV partial: this chunk's O (normalised by its own row
+                // sum) and LSE, fp32, into the workspace slot of the unit
+                const size_t slot = ((size_t)un.id * p.tpu + t) * kBM + row;
+                float* dst = p.ws_o + slot * D;
+                const uint32_t tO = tmem + lane_base + C::col_o(t);
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32_wait(tO + c0, o);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + c0 + i) =
+                            make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
+                                        __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                }
+                p.ws_lse[slot] = row_lse;
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t));
+                FA_TRACE_EV(leader, kTrEpilogue, kEvEpiDone, t);
+                continue;
+            }
             const int qrow = un.q_tile[t] * kBM + row;
-            if (qrow < p.S) p.lse[(size_t)un.bh * (size_t)p.S + (size_t)qrow] = (st.y + ptx::lg2(st.x)) * kLn2;
+            if (qrow < p.S) p.lse[(size_t)un.bh * (size_t)p.S + (size_t)qrow] = row_lse;
             const uint32_t tO = tmem + lane_base + C::col_o(t);
 #pragma unroll 1
             for (int box = 0; box < C::kBoxes; ++box) {
@@ -427,7 +487,7 @@ done:
 
 // ---------------------------------------------------------------------------------
 // TMA producer (one thread).
-template <int D>
+template <int D, bool kSplit>
 __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& wc, const CUtensorMap* tm_q,
                                           const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t smem_base,
                                           uint32_t bars)
@@ -439,7 +499,7 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
     bool ok = true;
     FA_TRACE_DECL;
     for (int r = 0; ok; ++r) {
-        const Unit un = unit_at(r, p);
+        const Unit un = unit_at<kSplit>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
 #pragma unroll
@@ -459,7 +519,7 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
             q_issued |= 1u << t;
             FA_TRACE_EV(true, kTrLoad, kEvQLoad, t);
         }
-        for (int j = 0; j < un.nmax && ok; ++j) {
+        for (int j = un.j0; j < un.nmax && ok; ++j) {
 #pragma unroll 1
             for (int kind = 0; kind < 2; ++kind) {
                 const uint32_t idx = kv_count;
@@ -495,7 +555,7 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
 
 // ---------------------------------------------------------------------------------
 // tcgen05 MMA issuer (one thread).
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kSplit>
 __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem, uint32_t smem_base,
                                          uint32_t bars)
 {
@@ -540,10 +600,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     };
 
     for (int r = 0;; ++r) {
-        const Unit un = unit_at(r, p);
+        const Unit un = unit_at<kSplit>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
-        const uint32_t kvb = kv_count;   // K_j is entry kvb + 2j of the ring, V_j is kvb + 2j + 1
+        // K_j is entry kvb + 2(j - j0) of the ring, V_j the entry after it
+        const uint32_t kvb = kv_count;
         FA_TRACE_EV(true, kTrMma, kEvUnit, un.id);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -559,11 +620,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             issue_qk(t, kvb);
             ptx::mma_commit(bars + 8 * (kBarSFull + t));
             FA_TRACE_EV(true, kTrMma, kEvQK, (uint32_t)t << 12);
-            if (un.nkv[t] == 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
+            if (un.nkv[t] == un.j0 + 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
         }
         kv_release(kvb);
-        for (int j = 0; j < un.nmax; ++j) {
-            const uint32_t iv = kvb + 2 * j + 1, ik = kvb + 2 * j + 2;
+        for (int j = un.j0; j < un.nmax; ++j) {
+            const uint32_t iv = kvb + 2 * (j - un.j0) + 1, ik = iv + 1;
             bool v_ready = false, k_ready = false;
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -572,7 +633,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     if (!ptx::mbar_wait(wc, bars + 8 * (kBarPHalf + t), (ph_ph >> t) & 1u, kSiteMma | (kBarPHalf + t)))
                         goto done;
                     ph_ph ^= 1u << t;
-                    if (j == 0) {
+                    if (j == un.j0) {
                         // O_t is overwritten: the previous unit's epilogue must have read it
                         if (!ptx::mbar_wait(wc, bars + 8 * (kBarOEmpty + t), ((ph_oe >> t) & 1u) ^ 1u,
                                             kSiteMma | (kBarOEmpty + t)))
@@ -584,7 +645,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                         v_ready = true;
                     }
                     ptx::tc_fence_after();
-                    issue_pv(t, iv, 0, j > 0);
+                    FA_TRACE_EV(true, kTrMma, kEvPVGo, ((uint32_t)t << 12) | j);
+                    issue_pv(t, iv, 0, j > un.j0);
+                    FA_TRACE_EV(true, kTrMma, kEvPVMid, ((uint32_t)t << 12) | j);
                     if (!ptx::mbar_wait(wc, bars + 8 * (kBarPFull + t), (ph_p >> t) & 1u, kSiteMma | (kBarPFull + t)))
                         goto done;
                     ph_p ^= 1u << t;
@@ -599,6 +662,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                         k_ready = true;
                         ptx::tc_fence_after();
                     }
+                    FA_TRACE_EV(true, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
                     issue_qk(t, ik);
                     ptx::mma_commit(bars + 8 * (kBarSFull + t));
                     FA_TRACE_EV(true, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
@@ -608,7 +672,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             if (j + 1 < un.nmax) kv_release(ik);
             kv_release(iv);
         }
-        kv_count = kvb + 2 * un.nmax;
+        kv_count = kvb + 2 * (un.nmax - un.j0);
     }
 done:
     // every MMA must be complete before tensor memory is released
@@ -617,7 +681,7 @@ done:
 }
 
 // ---------------------------------------------------------------------------------
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -633,6 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(smem + C::kOffCtl);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    FA_TRACE_DECL;
+    FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvEntry, 0);
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -669,35 +735,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = ctl[0];
     const ptx::WaitCtx wc{base + C::kOffCtl + 4, p.timeout_ns, p.status};
+    FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvSetup, 0);
 
     if (warp < 8) {
-        ptx::setmaxnreg_inc<RegSplit<D>::kSoftmax>();
-        softmax_role<D, kBF16>(p, wc, warp >> 2, tmem, bars, stats);
+        ptx::setmaxnreg_inc<RegSplit<D, kSplit>::kSoftmax>();
+        softmax_role<D, kBF16, kSplit>(p, wc, warp >> 2, tmem, bars, stats);
     } else if (warp < 12) {
-        ptx::setmaxnreg_dec<RegSplit<D>::kEpilogue>();
-        correction_epilogue_role<D, kBF16>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
+        ptx::setmaxnreg_dec<RegSplit<D, kSplit>::kEpilogue>();
+        correction_epilogue_role<D, kBF16, kSplit>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
     } else {
-        ptx::setmaxnreg_dec<RegSplit<D>::kControl>();
+        ptx::setmaxnreg_dec<RegSplit<D, kSplit>::kControl>();
         if (warp == 12) {
-            if (lane == 0) load_role<D>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
+            if (lane == 0) load_role<D, kSplit>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {
-            if (lane == 0) mma_role<D, kBF16>(p, wc, tmem, base, bars);
+            if (lane == 0) mma_role<D, kBF16, kSplit>(p, wc, tmem, base, bars);
         }
         __syncwarp();
     }
 
     ptx::tc_fence_before();
     __syncthreads();
+    FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvExit, 0);
     if (warp == 13) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
 }
 
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kSplit>
 int launch_instance(const LaunchArgs& a, cudaStream_t stream)
 {
-    auto kern = fa_fwd_kernel<D, kBF16>;
+    auto kern = fa_fwd_kernel<D, kBF16, kSplit>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
     if (e != cudaSuccess) return (int)e;
     cudaLaunchConfig_t cfg = {};

@@ -1,0 +1,6 @@
+// Kernel instance: head dim 64, f16 inputs/outputs, split over key chunks.
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+int launch_d64_f16_split(const LaunchArgs& a, cudaStream_t s) { return launch_instance<64, false, true>(a, s); }
+}  // namespace fa
