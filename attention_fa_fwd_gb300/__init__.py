@@ -19,12 +19,13 @@ import torch
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_splitkv", "splitkv_workspace_bytes", "fa_fwd_hostio", "launch_info", "plan", "device_status",
+__all__ = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "splitkv_workspace_bytes", "fa_fwd_hostio", "launch_info", "plan", "device_status",
            "selftest_wait_timeout", "strerror", "build", "lib", "header_functions",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
-           "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FaError"]
+           "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_SCRATCH", "FaError"]
 
-FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
+(FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_TIMEOUT,
+ FA_ERR_SCRATCH) = range(7)
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
 HEADER = os.path.join(_build.ROOT, "include", "fa_fwd.h")
 
@@ -64,6 +65,7 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_hostio.argtypes = [vp] * 10 + dims
         L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
         L.fa_fwd_splitkv_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        L.fa_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp] + dims
         L.fa_fwd_launch_info.argtypes = [i, i, i, i, i, i, ctypes.POINTER(LaunchInfo)]
         L.fa_fwd_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(LaunchInfo)]
         L.fa_device_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint)]
@@ -72,7 +74,7 @@ def lib() -> ctypes.CDLL:
         L.fa_strerror.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_fwd_hostio", "fa_fwd_launch_info", "fa_fwd_plan",
                      "fa_device_status", "fa_selftest_wait_timeout", "fa_fwd_splitkv",
-                     "fa_fwd_splitkv_workspace"):
+                     "fa_fwd_splitkv_workspace", "fa_fwd_splitkv_static"):
             getattr(L, name).restype = i
         _lib = L
     return _lib
@@ -177,6 +179,30 @@ def fa_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bo
                                   _stream_ptr(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_splitkv")
+    return out, lse
+
+
+def fa_fwd_splitkv_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                          scale: float | None = None, out: torch.Tensor | None = None,
+                          lse: torch.Tensor | None = None, stream=None):
+    """fa_fwd_splitkv without a workspace: for callers that cannot allocate
+    device memory, the split scratch is a fixed 32 MiB array inside the library
+    (shared by every call on a device; overlapping calls race on it).  Raises
+    FaError with FA_ERR_SCRATCH when the problem needs more than that."""
+    _check_qkv(q, k, v)
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        rc = lib().fa_fwd_splitkv_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                         lse.data_ptr(), B, H, S, D, int(bool(causal)), float(scale),
+                                         _DTYPE[q.dtype], _stream_ptr(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv_static")
     return out, lse
 
 

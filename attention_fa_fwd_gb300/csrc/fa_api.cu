@@ -298,6 +298,7 @@ const char* fa_strerror(int status)
     case FA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
     case FA_ERR_CUDA: return "CUDA runtime/driver error";
     case FA_ERR_TIMEOUT: return "a bounded in-kernel wait timed out";
+    case FA_ERR_SCRATCH: return "problem needs more split-KV scratch than the library's static array holds";
     default: return "unknown status";
     }
 }
@@ -515,3 +516,50 @@ int fa_trace_set(unsigned long long* buf, int ctas, int cap)
 #endif
 
 }  // extern "C"
+
+// ---- split-KV without allocation -------------------------------------------------
+// Scratch for fa_fwd_splitkv_static: a file-scope device array, so a caller
+// that cannot allocate device memory still gets the split path.  Each device
+// that loads the library holds these bytes until the process exits.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = 32ull << 20;   // 32 MiB
+
+static __device__ __align__(256) unsigned char g_fa_static_scratch[kStaticScratchBytes];
+
+// Device address of the array, looked up once per device (with that device
+// current) and cached; in host code the symbol itself is not a device address.
+std::atomic<void*> g_static_scratch_ptr[kMaxDevices];
+
+int static_scratch(void** ptr)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    void* p = g_static_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        if (cudaGetSymbolAddress(&p, g_fa_static_scratch) != cudaSuccess || !p) return FA_ERR_CUDA;
+        g_static_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
+    *ptr = p;
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                     int S, int D, int causal, float scale, int dtype, void* stream)
+{
+    int num_sms = 0;
+    int rc = check_call(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, &num_sms);
+    if (rc != FA_OK) return rc;
+    SplitPlan sp;
+    if (!plan_split(B * H, S, causal, num_sms, &sp))
+        return run_fwd(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, num_sms, nullptr, nullptr, stream);
+    if (split_workspace_bytes(sp, D) > kStaticScratchBytes) return FA_ERR_SCRATCH;
+    void* ws = nullptr;
+    rc = static_scratch(&ws);
+    if (rc != FA_OK) return rc;
+    return run_fwd(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, num_sms, &sp, static_cast<float*>(ws), stream);
+}

@@ -57,7 +57,8 @@ typedef enum {
     FA_ERR_UNSUPPORTED = 2,  /* D not in {64, 128}, unknown dtype, no sm_100-family device */
     FA_ERR_MISALIGNED = 3,   /* a tensor pointer not 16-byte aligned */
     FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, copy, tensor map) */
-    FA_ERR_TIMEOUT = 5       /* a bounded in-kernel wait gave up (reported by fa_device_status) */
+    FA_ERR_TIMEOUT = 5,      /* a bounded in-kernel wait gave up (reported by fa_device_status) */
+    FA_ERR_SCRATCH = 6       /* fa_fwd_splitkv_static: the problem needs more than its static scratch */
 } fa_status_t;
 
 /*
@@ -108,6 +109,32 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
  * Host only; errors as fa_fwd's argument checks.
  */
 int fa_fwd_splitkv_workspace(int B, int H, int S, int D, int causal, int dtype, size_t* bytes);
+
+/*
+ * fa_fwd_splitkv_static - fa_fwd_splitkv for callers that cannot allocate.
+ *
+ * No counterpart on the source pages: this entry point exists for callers that
+ * must not or cannot call cudaMalloc - runtimes that forbid allocation after
+ * start-up (fixed memory budgets, real-time serving loops), or code that runs
+ * under another framework's allocator and holds no handle to it - but still
+ * want the split path for small problems.  It allocates nothing: its split
+ * scratch is a static device array of 32 MiB (2^25 bytes) inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ * Same arguments, layouts and results as fa_fwd_splitkv, without the
+ * workspace.  The first call on a device looks up that device's address of the
+ * array (cudaGetSymbolAddress, with the device current) and caches it; make
+ * that first call before any stream capture.  All calls on a device share the
+ * one array: calls whose work overlaps on the GPU (different streams, or
+ * threads) race on it and must be serialised by the caller.  The array keeps
+ * the last call's partial results; nothing in it needs clearing, since a call
+ * writes every partial it reads.  Returns FA_ERR_SCRATCH, launching nothing,
+ * when the split plan needs more than 32 MiB (fa_fwd_splitkv_workspace reports
+ * the need); otherwise errors as fa_fwd_splitkv.  Problems that one pass
+ * already fits run as fa_fwd and use no scratch.
+ */
+int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int H, int S, int D, int causal, float scale, int dtype, void* stream);
 
 /*
  * fa_fwd_hostio - the same pass with host-side inputs and outputs.
