@@ -574,13 +574,18 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + idx % C::kSlots)); };
     // S_t = Q_t K^T: M = 128 rows, N = 128 keys, K = D in steps of 16 (32 bytes
     // inside a 128-byte swizzled row; the next 64 columns sit in the next box).
+    // Descriptors are built once per tile and stepped by adding the offset to
+    // the start-address field of their low word: the issuing thread's
+    // instructions per MMA are part of what keeps the tensor pipe fed
+    // (measured: +4.5% against rebuilding each descriptor).
+    constexpr uint32_t kDescHi = ptx::sdesc_hi_sw128(1024);
     auto issue_qk = [&](int t, uint32_t idx) {
-        const uint32_t qa = smem_base + C::kOffQ + t * C::kTileBytes;
-        const uint32_t kb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes;
+        const uint32_t qa = ptx::sdesc_lo(smem_base + C::kOffQ + t * C::kTileBytes, 16);
+        const uint32_t kb = ptx::sdesc_lo(smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes, 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-            ptx::mma_ss(tmem + C::col_s(t), ptx::sdesc_sw128(qa + off, 16, 1024), ptx::sdesc_sw128(kb + off, 16, 1024),
+            const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            ptx::mma_ss(tmem + C::col_s(t), ptx::sdesc_join(qa + off, kDescHi), ptx::sdesc_join(kb + off, kDescHi),
                         kIdescQK, kk > 0 ? 1u : 0u);
         }
     };
@@ -590,12 +595,12 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     // One half: keys 64*half .. 64*half+63 (four K=16 steps).
     auto issue_pv = [&](int t, uint32_t idx, int half, bool acc) {
         const uint32_t vb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes;
+        const uint32_t vl = ptx::sdesc_lo(vb, C::kBoxBytes);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = half * 4 + k4;
             ptx::mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
-                        ptx::sdesc_sw128(vb + kk * 16 * 128, C::kBoxBytes, 1024), kIdescPV,
-                        (acc || kk > 0) ? 1u : 0u);
+                        ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
     };
 

@@ -253,15 +253,27 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4
 //   bits 32-45 stride byte offset >> 4 bits 46-47 descriptor version (1)
 //   bits 61-63 layout: 2 = 128-byte swizzle
+// The low word (start address, leading byte offset) is what changes from one
+// operand to the next; the high word is fixed by the layout.  Issuers that
+// step through a tile keep only the low word and add start-address steps to
+// it (a shared address below 256 KB never carries out of its 14 bits).
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo)
+{
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo)
+{
+    return ((sbo >> 4) & 0x3FFFu) | (1u << (46 - 32)) | (2u << (61 - 32));
+}
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo, uint32_t hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
 {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
+    return sdesc_join(sdesc_lo(saddr, lbo), sdesc_hi_sw128(sbo));
 }
 
 // Instruction descriptor of kind::f16 with fp32 accumulation.
