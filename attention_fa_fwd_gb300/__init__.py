@@ -70,10 +70,11 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(LaunchInfo)]
         L.fa_device_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint)]
         L.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        L.fa_selftest_exp2_poly.argtypes = [vp, vp, i, vp]
         L.fa_strerror.argtypes = [i]
         L.fa_strerror.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_fwd_hostio", "fa_fwd_launch_info", "fa_fwd_plan",
-                     "fa_device_status", "fa_selftest_wait_timeout", "fa_fwd_splitkv",
+                     "fa_device_status", "fa_selftest_wait_timeout", "fa_selftest_exp2_poly", "fa_fwd_splitkv",
                      "fa_fwd_splitkv_workspace", "fa_fwd_splitkv_static"):
             getattr(L, name).restype = i
         _lib = L
@@ -262,3 +263,16 @@ def selftest_wait_timeout(timeout_us: int, stream=None) -> None:
     rc = lib().fa_selftest_wait_timeout(int(timeout_us), _stream_ptr(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_selftest_wait_timeout")
+
+
+def selftest_exp2_poly(x, stream=None):
+    """2^x by the FMA-pipe exponential, element-wise, for a CUDA float32 tensor."""
+    import torch
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32):
+        raise TypeError("x must be a CUDA float32 tensor")
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    rc = lib().fa_selftest_exp2_poly(x.data_ptr(), y.data_ptr(), x.numel(), _stream_ptr(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_selftest_exp2_poly")
+    return y

@@ -502,6 +502,15 @@ int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream)
     return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+int fa_selftest_exp2_poly(const float* x, float* y, int n, void* stream)
+{
+    if (n < 0 || (n > 0 && (x == nullptr || y == nullptr))) return FA_ERR_INVALID_ARG;
+    if (n == 0) return FA_OK;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % alignof(float) != 0) return FA_ERR_MISALIGNED;
+    const int e = fa::launch_exp2_poly_selftest(x, y, n, static_cast<cudaStream_t>(stream));
+    return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 #ifdef FA_TRACE
 // Trace build only: every later fa_fwd records events of CTAs [0, ctas) into
 // `buf` (device, ctas * 6 * cap 64-bit words, caller-owned, zeroed by the caller).

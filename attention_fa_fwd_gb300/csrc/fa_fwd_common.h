@@ -120,5 +120,6 @@ int smem_bytes_for(int D);
 
 // Kernel that waits on a barrier nobody arrives on (bounded-wait self-test).
 int launch_wait_selftest(unsigned int* status, unsigned long long timeout_ns, cudaStream_t s);
+int launch_exp2_poly_selftest(const float* x, float* y, int n, cudaStream_t s);
 
 }  // namespace fa

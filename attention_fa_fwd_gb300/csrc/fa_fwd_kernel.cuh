@@ -58,6 +58,17 @@
 namespace fa {
 
 constexpr float kRebaseThreshold = 8.0f;   // log2 units ("G6", V41: base + 8)
+
+// Pairs out of every 16 whose exponentials use ptx::f2_exp2_poly (the FMA
+// pipe) instead of ex2.approx (the XU): the split of the exponential work the
+// "Triton" page's MIO-bottleneck section motivates.  Off by default: on GB300
+// the XU retires ex2 fast enough that the extra FMA-pipe instructions cost
+// more than they save (the build option exists to measure that).
+#ifndef FA_EXP2_POLY_PAIRS
+#define FA_EXP2_POLY_PAIRS 0
+#endif
+constexpr int kExp2PolyPairs = FA_EXP2_POLY_PAIRS;
+static_assert(kExp2PolyPairs >= 0 && kExp2PolyPairs <= 16, "FA_EXP2_POLY_PAIRS must be in [0, 16]");
 constexpr float kLn2 = 0.693147180559945309f;
 
 // Register budget per warpgroup after setmaxnreg: softmax x2, epilogue, control
@@ -340,7 +351,13 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 for (int i = 0; i < 16; ++i) {
                     float x0, x1;
                     ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nb2), x0, x1);
-                    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                    float p0, p1;
+                    if (kExp2PolyPairs > 0 && ((i + 1) * kExp2PolyPairs / 16) != (i * kExp2PolyPairs / 16)) {
+                        ptx::f2_unpack(ptx::f2_exp2_poly(x0, x1), p0, p1);   // spread evenly over the 16 pairs
+                    } else {
+                        p0 = ptx::ex2(x0);
+                        p1 = ptx::ex2(x1);
+                    }
                     acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
                     pk[i] = ptx::pack2<kBF16>(p0, p1);
                 }

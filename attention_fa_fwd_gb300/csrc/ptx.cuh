@@ -429,6 +429,32 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
     return r;
 }
 
+// 2^x for a pair of floats on the FMA pipe instead of the XU (MUFU).
+//   x = n + f, n = rint(x): adding M = 1.5 * 2^23 + 127 rounds x to an integer
+//   and leaves n + 127 in the low bits of the sum t; t - M = n exactly; f in
+//   [-1/2, 1/2].  2^f: degree-3 polynomial minimising the relative error on
+//   [-1/2, 1/2] (Remez exchange; attention_fa_fwd_gb300/exp2_poly_fit.py
+//   prints these coefficients; max relative error 7.5e-5).  2^n: the low nine
+//   bits of t shifted to the exponent field, which is exactly 2^n for n in
+//   [-127, 128] (n = -127 gives +0).  x is clamped at -127 first, so -inf and
+//   very negative arguments give 0, as ex2.approx.ftz does.  Results below
+//   2^-126 flush to zero (the final multiply is .ftz).
+__device__ __forceinline__ uint64_t f2_exp2_poly(float x0, float x1)
+{
+    constexpr float kM = 12583039.0f;   // 1.5 * 2^23 + 127
+    constexpr float kC0 = 0.9999280572f, kC1 = 0.6932609677f, kC2 = 0.2426111251f, kC3 = 0.05517166853f;
+    const uint64_t x = f2_pack(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
+    const uint64_t t = f2_add(x, f2_pack(kM, kM));
+    const uint64_t n = f2_add(t, f2_pack(-kM, -kM));
+    const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), x);
+    uint64_t p = f2_fma(f, f2_pack(kC3, kC3), f2_pack(kC2, kC2));
+    p = f2_fma(p, f, f2_pack(kC1, kC1));
+    p = f2_fma(p, f, f2_pack(kC0, kC0));
+    float t0, t1;
+    f2_unpack(t, t0, t1);
+    return f2_mul(p, f2_pack(__uint_as_float(__float_as_uint(t0) << 23), __uint_as_float(__float_as_uint(t1) << 23)));
+}
+
 // max of three fp32 values in one instruction
 __device__ __forceinline__ float max3(float a, float b, float c)
 {

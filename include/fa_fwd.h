@@ -198,6 +198,25 @@ int fa_device_status(void* stream, int clear, unsigned int* site);
  */
 int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream);
 
+/*
+ * fa_selftest_exp2_poly - evaluates the FMA-pipe exponential the softmax can
+ * use for part of its exponentials (build option FA_EXP2_POLY_PAIRS; off in
+ * the default build): y[i] = 2^x[i] for i < n.
+ *
+ * The method is the range reduction 2^x = 2^n * 2^f (n = rint(x),
+ * f in [-1/2, 1/2]) with a degree-3 minimax polynomial for 2^f; the split of
+ * the exponential work between units follows the MIO-bottleneck section of
+ * "FlashAttention的Triton性能考古学".  Relative error <= 7.5e-5 for results
+ * >= 2^-126 (x >= -125.9); arguments <= -127 (and -inf) give +0.
+ *
+ * x, y: device pointers to n floats (4-byte aligned), caller-owned; n >= 0
+ * (n = 0 launches nothing).  Enqueued on `stream`, returns at once.
+ * FA_ERR_INVALID_ARG for n < 0 or a null pointer with n > 0,
+ * FA_ERR_MISALIGNED for a pointer not 4-byte aligned, FA_ERR_CUDA if the
+ * launch fails.
+ */
+int fa_selftest_exp2_poly(const float* x, float* y, int n, void* stream);
+
 /* Human-readable text for an fa_status_t; never NULL. */
 const char* fa_strerror(int status);
 
