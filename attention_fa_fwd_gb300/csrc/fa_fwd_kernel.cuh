@@ -32,8 +32,11 @@
 // split), so half of P*V overlaps the second half of the exponentials.
 //
 // Softmax uses the conditional rescale of "G6", V41, in the base-2 domain: the
-// row base b only moves when the tile maximum exceeds b + 8, so p = 2^(x - b)
-// lies in (0, 256].  The row maximum of an unmasked tile comes with the TMEM
+// row base b only moves when the tile maximum exceeds b + T, so p = 2^(x - b)
+// lies in (0, 2^T].  The page uses T = 8 with fp16 P summed in half2; here P is
+// summed in fp32, so T is set by P's type alone: 15 for fp16 (2^15 < 65504)
+// and 30 for bf16 (fp32's exponent range), which makes rescales much rarer on
+// inputs whose row maxima keep rising.  The row maximum of an unmasked tile comes with the TMEM
 // load (tcgen05.ld.red .max; "G6", V41: "4 ld.red").  When a row's base moves,
 // the softmax warp owning it rescales its 32 rows of O in TMEM before it
 // publishes P ("G6", V44: the rescale moved into the softmax warpgroups; here
@@ -57,7 +60,10 @@
 
 namespace fa {
 
-constexpr float kRebaseThreshold = 8.0f;   // log2 units ("G6", V41: base + 8)
+// Re-base threshold T in log2 units ("G6", V41 uses base + 8): p <= 2^T must be
+// finite in P's 16-bit type; the row sums and O accumulate in fp32.
+template <bool kBF16>
+__host__ __device__ constexpr float rebase_threshold() { return kBF16 ? 30.0f : 15.0f; }
 
 // Pairs out of every 16 whose exponentials use ptx::f2_exp2_poly (the FMA
 // pipe) instead of ex2.approx (the XU): the split of the exponential work the
@@ -73,19 +79,24 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 // Register budget per warpgroup after setmaxnreg: softmax x2, epilogue, control
 // (load + MMA).  The four add up to 512 = 65536 registers / 128 threads; the
-// splits are the spill-free ones ptxas -v reports for each head dim.
-template <int D, bool kSplit> struct RegSplit;
-template <> struct RegSplit<128, false> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 64, kControl = 96; };
-template <> struct RegSplit<64, false> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 72, kControl = 88; };
-template <> struct RegSplit<128, true> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 48, kControl = 96; };
-template <> struct RegSplit<64, true> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 48, kControl = 96; };
-template <int D, bool kSplit>
+// splits are the spill-free ones ptxas -v reports for each head dim and type.
+template <int D, bool kBF16, bool kSplit> struct RegSplit {   // split-KV kernels
+    static constexpr uint32_t kSoftmax = 184, kEpilogue = 48, kControl = 96;
+};
+template <> struct RegSplit<128, false, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80; };
+template <> struct RegSplit<128, true, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80; };
+template <> struct RegSplit<64, false, false> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 72, kControl = 88; };
+template <> struct RegSplit<64, true, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72; };
+template <int D, bool kBF16, bool kSplit>
 constexpr bool reg_split_fits()
 {
-    return 2 * RegSplit<D, kSplit>::kSoftmax + RegSplit<D, kSplit>::kEpilogue + RegSplit<D, kSplit>::kControl == 512;
+    using R = RegSplit<D, kBF16, kSplit>;
+    return 2 * R::kSoftmax + R::kEpilogue + R::kControl == 512;
 }
-static_assert(reg_split_fits<128, false>() && reg_split_fits<64, false>(), "register split must add up to 512");
-static_assert(reg_split_fits<128, true>() && reg_split_fits<64, true>(), "register split must add up to 512");
+static_assert(reg_split_fits<128, false, false>() && reg_split_fits<128, true, false>() &&
+                  reg_split_fits<64, false, false>() && reg_split_fits<64, true, false>() &&
+                  reg_split_fits<128, false, true>() && reg_split_fits<64, true, true>(),
+              "register split must add up to 512");
 
 // Barrier indices inside the barrier array.
 enum : int {
@@ -112,10 +123,10 @@ struct Cfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
     static constexpr int kOffStage = kOffKV + kSlots * kTileBytes;   // one O box for the TMA store
-    static constexpr int kOffStats = kOffStage + kBoxBytes;          // float2 (l, b) [2][128]
+    static constexpr int kOffStats = kOffStage + kBoxBytes;          // float4 (l, b, l_norm, 0) [2][128]
     static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
     static constexpr int kNumBars = kBarKVEmpty + kSlots;
-    static constexpr int kOffBars = kOffStats + 2 * kBM * 8;
+    static constexpr int kOffBars = kOffStats + 2 * kBM * 16;
     static constexpr int kOffCtl = kOffBars + kNumBars * 8;          // [0] TMEM base, [1] abort, [2] epilogue go
     static constexpr int kSmemBytes = kOffCtl + 16 + 1024;            // + slack to align the base to 1 KB
     // TMEM columns of the score region S_t and the output accumulator O_t
@@ -253,7 +264,7 @@ enum : uint32_t { kSiteSoftmax = 0x100, kSiteEpilogue = 0x300, kSiteLoad = 0x400
 // Softmax warpgroup t: one thread per query row of tile t.
 template <int D, bool kBF16, bool kSplit>
 __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx& wc, int t, uint32_t tmem,
-                                             uint32_t bars, float2* stats)
+                                             uint32_t bars, float4* stats)
 {
     using C = Cfg<D>;
     const int lane = threadIdx.x & 31;
@@ -278,7 +289,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
         const int last = kSplit ? (t ? un.last[1] : un.last[0]) : nkv - 1;
         if (nkv == 0) continue;
         float b = -INFINITY;   // base of the row, base-2 scaled units
-        float l = 0.f;         // running sum of 2^(x - b)
+        float l = 0.f;         // running sum of 2^(x - b): gives the LSE
+        // bf16: O is normalised by l + dl, where dl sums, per key tile, the
+        // rounding of the tile's largest p to bf16.  The MMAs weight V with the
+        // rounded P; when one key dominates a row, its rounding (up to 2^-9
+        // relative) would otherwise scale that row of O, and O rounded to bf16
+        // has no room left for it in the |dO| budget.  (fp16 rounds P to 2^-12
+        // and O to 2^-11 relative: dl stays 0 there.)
+        float dl = 0.f;
         for (int j = un.j0; j < nkv; ++j) {
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + t), ph_s, kSiteSoftmax | (kBarSFull + t))) return;
             ph_s ^= 1u;
@@ -318,16 +336,22 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 mraw = fmaxf(ptx::max3(pm[0], pm[1], pm[2]), pm[3]);
             }
             const float mx = mraw * sl2;
-            // conditional re-base: keep b unless the maximum passed b + 8
-            float h = 1.f;
+            // conditional re-base: keep b unless the maximum passed b + T.  The O
+            // rescale below is warp-wide (collective TMEM accesses), so when one
+            // row of the warp re-bases, every row of the warp re-bases to its
+            // own candidate at no extra cost: all 32 restart with the full
+            // margin, and the next warp rescale waits for a row to climb T more.
             const float cand = fmaxf(b, mx);
-            if (cand > b + kRebaseThreshold) {
-                h = ptx::ex2(b - cand);   // 0 on the first tile (b = -inf)
+            const bool rebase = cand > b + rebase_threshold<kBF16>();
+            const bool rescale = j > un.j0 && __any_sync(0xffffffffu, rebase);
+            float h = 1.f;
+            if (rebase || rescale) {
+                h = ptx::ex2(b - cand);   // 0 on the first tile (b = -inf); 1 if cand == b
                 b = cand;
             }
             FA_TRACE_EV(tr, t, kEvMaxDone, j);
-            if (j > un.j0 && __any_sync(0xffffffffu, h < 1.f)) {
-                // rare path: this warp's 32 rows of O_t are scaled by 2^(b_old - b_new)
+            if (rescale) {
+                // this warp's 32 rows of O_t are scaled by 2^(b_old - b_new)
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
@@ -344,6 +368,11 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             const float nb = (b == -INFINITY) ? 0.f : -b;
             const uint64_t c2 = ptx::f2_pack(sl2, sl2), nb2 = ptx::f2_pack(nb, nb);
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+            if constexpr (kBF16) {
+                // the tile maximum's p, by the same FMA and ex2 the loop below uses
+                const float pm = ptx::ex2(fmaf(mraw, sl2, nb));
+                dl = fmaf(dl, h, ptx::round16<kBF16>(pm) - pm);
+            }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
@@ -380,7 +409,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
         if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarStEmpty + t), ph_te ^ 1u, kSiteSoftmax | (kBarStEmpty + t)))
             return;
         ph_te ^= 1u;
-        stats[t * kBM + row] = make_float2(l, b);
+        stats[t * kBM + row] = make_float4(l, b, l + dl, 0.f);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarStFull + t));
     }
@@ -392,7 +421,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
 template <int D, bool kBF16, bool kSplit>
 __device__ __forceinline__ void correction_epilogue_role(const Params& p, const ptx::WaitCtx& wc,
                                                          const CUtensorMap* tm_o, uint32_t tmem, uint32_t smem_base,
-                                                         uint32_t bars, const float2* stats, volatile uint32_t* ctl_go)
+                                                         uint32_t bars, const float4* stats, volatile uint32_t* ctl_go)
 {
     using C = Cfg<D>;
     const int lane = threadIdx.x & 31;
@@ -427,10 +456,10 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             ph_t ^= 1u << t;
             FA_TRACE_EV(leader, kTrEpilogue, kEvOFull, t);
             ptx::tc_fence_after();
-            const float2 st = stats[t * kBM + row];
+            const float4 st = stats[t * kBM + row];
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarStEmpty + t));
-            const float inv_l = 1.0f / st.x;
+            const float inv_l = 1.0f / st.z;   // the sum of the P values the MMAs used
             const float row_lse = (st.y + ptx::lg2(st.x)) * kLn2;
             if constexpr (kSplit) {
                 // split-KV partial: this chunk's O (normalised by its own row
@@ -715,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw);
     const uint32_t bars = base + C::kOffBars;
-    float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
+    float4* stats = reinterpret_cast<float4*>(smem + C::kOffStats);
     volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(smem + C::kOffCtl);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -760,13 +789,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvSetup, 0);
 
     if (warp < 8) {
-        ptx::setmaxnreg_inc<RegSplit<D, kSplit>::kSoftmax>();
+        ptx::setmaxnreg_inc<RegSplit<D, kBF16, kSplit>::kSoftmax>();
         softmax_role<D, kBF16, kSplit>(p, wc, warp >> 2, tmem, bars, stats);
     } else if (warp < 12) {
-        ptx::setmaxnreg_dec<RegSplit<D, kSplit>::kEpilogue>();
+        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit>::kEpilogue>();
         correction_epilogue_role<D, kBF16, kSplit>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
     } else {
-        ptx::setmaxnreg_dec<RegSplit<D, kSplit>::kControl>();
+        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit>::kControl>();
         if (warp == 12) {
             if (lane == 0) load_role<D, kSplit>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {

@@ -476,5 +476,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     return d;
 }
 
+// x rounded to the 16-bit type (nearest even), returned as fp32: the value an
+// element packed by pack2 carries into the MMA.
+template <bool kBF16>
+__device__ __forceinline__ float round16(float x)
+{
+    const uint32_t d = pack2<kBF16>(x, x);
+    if constexpr (kBF16) {
+        return __uint_as_float(d << 16);   // a bf16 is the upper half of the fp32 with its value
+    } else {
+        float r;
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(r) : "r"(d));
+        return r;
+    }
+}
+
 }  // namespace ptx
 }  // namespace fa
