@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/fa_fwd.h: argument checks, TMA
 // tensor maps, launch geometry and the work-unit schedule, dispatch to the
 // kernel instances.  Nothing here allocates device memory.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -453,6 +454,54 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    stream);
 }
 
+namespace {
+
+// The pipelined host-buffer path: the B*H heads are cut into chunks of whole
+// heads (a multiple of 4, so every chunk's LSE slice stays 16-byte aligned)
+// and the chunks go round-robin over a few library-owned streams, so chunk
+// c+1 uploads while chunk c computes and chunk c-1 downloads.  Streams and
+// events are host objects created once per device; nothing is allocated on
+// the device.  The enqueue is serialised per device, so the shared events
+// are recorded and waited on in matching pairs.
+constexpr int kIoStreams = 3;
+constexpr int kIoMaxChunks = 8;
+constexpr size_t kIoMinBytes = size_t(32) << 20;     // below this one pass is enqueued as is
+constexpr size_t kIoChunkBytes = size_t(48) << 20;   // input bytes per chunk, about
+
+struct IoPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t st[kIoStreams];
+    cudaEvent_t start, done[kIoStreams];
+};
+IoPipe g_io[kMaxDevices];
+
+int io_pipe_init(IoPipe& io)
+{
+    if (io.ready) return FA_OK;
+    for (int i = 0; i < kIoStreams; ++i)
+        if (cudaStreamCreateWithFlags(&io.st[i], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&io.done[i], cudaEventDisableTiming) != cudaSuccess)
+            return FA_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&io.start, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
+    io.ready = true;
+    return FA_OK;
+}
+
+// Heads per chunk for a pass of BH heads; 0 means "do not chunk".
+int io_heads_per_chunk(int BH, size_t head_bytes)
+{
+    const size_t in_bytes = 3 * (size_t)BH * head_bytes;
+    if (BH < 8 || in_bytes < kIoMinBytes) return 0;
+    int chunks = (int)std::min<size_t>(kIoMaxChunks, std::max<size_t>(2, in_bytes / kIoChunkBytes));
+    chunks = std::min(chunks, BH / 4);
+    if (chunks < 2) return 0;
+    const int hc = ((BH + chunks - 1) / chunks + 3) / 4 * 4;
+    return hc < BH ? hc : 0;
+}
+
+}  // namespace
+
 int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, void* q_d, void* k_d,
                   void* v_d, void* o_d, float* lse_d, int B, int H, int S, int D, int causal, float scale, int dtype,
                   void* stream)
@@ -467,6 +516,48 @@ int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
         if (!aligned16(p)) return FA_ERR_MISALIGNED;
     const size_t n = (size_t)B * H * S * D * 2, nl = (size_t)B * H * S * sizeof(float);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int BH = B * H;
+    const size_t head_bytes = (size_t)S * D * 2, head_lse = (size_t)S * sizeof(float);
+    const int hc = io_heads_per_chunk(BH, head_bytes);
+    if (hc > 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+        IoPipe& io = g_io[dev];
+        std::lock_guard<std::mutex> lock(io.mu);
+        if ((rc = io_pipe_init(io)) != FA_OK) return rc;
+        // the chunks start after the caller's earlier work on `stream` ...
+        if (cudaEventRecord(io.start, s) != cudaSuccess) return FA_ERR_CUDA;
+        for (int i = 0; i < kIoStreams; ++i)
+            if (cudaStreamWaitEvent(io.st[i], io.start, 0) != cudaSuccess) return FA_ERR_CUDA;
+        auto at = [](const void* base, size_t off) {
+            return static_cast<char*>(const_cast<void*>(base)) + off;
+        };
+        int used = 0;
+        for (int h0 = 0, c = 0; h0 < BH; h0 += hc, ++c) {
+            const int nh = std::min(hc, BH - h0);
+            cudaStream_t cs = io.st[c % kIoStreams];
+            used = std::max(used, c % kIoStreams + 1);
+            const size_t off = (size_t)h0 * head_bytes, bytes = (size_t)nh * head_bytes;
+            const size_t loff = (size_t)h0 * head_lse, lbytes = (size_t)nh * head_lse;
+            if (cudaMemcpyAsync(at(q_d, off), at(q_h, off), bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+                cudaMemcpyAsync(at(k_d, off), at(k_h, off), bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+                cudaMemcpyAsync(at(v_d, off), at(v_h, off), bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+                return FA_ERR_CUDA;
+            // heads are independent: a chunk is the pass of B = 1, H = nh on its slices
+            rc = fa_fwd(at(q_d, off), at(k_d, off), at(v_d, off), at(o_d, off),
+                        reinterpret_cast<float*>(at(lse_d, loff)), 1, nh, S, D, causal, scale, dtype, cs);
+            if (rc != FA_OK) return rc;
+            if (cudaMemcpyAsync(at(o_h, off), at(o_d, off), bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+                cudaMemcpyAsync(at(lse_h, loff), at(lse_d, loff), lbytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+                return FA_ERR_CUDA;
+        }
+        // ... and the caller's later work on `stream` waits for all of them
+        for (int i = 0; i < used; ++i)
+            if (cudaEventRecord(io.done[i], io.st[i]) != cudaSuccess ||
+                cudaStreamWaitEvent(s, io.done[i], 0) != cudaSuccess)
+                return FA_ERR_CUDA;
+        return FA_OK;
+    }
     if (cudaMemcpyAsync(q_d, q_h, n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(k_d, k_h, n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(v_d, v_h, n, cudaMemcpyHostToDevice, s) != cudaSuccess)

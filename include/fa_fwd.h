@@ -139,12 +139,21 @@ int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, 
 /*
  * fa_fwd_hostio - the same pass with host-side inputs and outputs.
  *
- * Enqueues on `stream`: host->device copies of q_h, k_h, v_h into the caller's
- * device buffers q_d, k_d, v_d; fa_fwd on them into o_d, lse_d; device->host
- * copies of o_d, lse_d into o_h, lse_h.  Returns once everything is enqueued;
- * the caller synchronises `stream` before reading o_h / lse_h.  Host buffers
- * should be pinned for the copies to be asynchronous.  Same layouts, sizes and
- * errors as fa_fwd; all ten pointers must be non-null and 16-byte aligned.
+ * Host->device copies of q_h, k_h, v_h into the caller's device buffers q_d,
+ * k_d, v_d; fa_fwd on them into o_d, lse_d; device->host copies of o_d, lse_d
+ * into o_h, lse_h.  Returns once everything is enqueued; the caller
+ * synchronises `stream` before reading o_h / lse_h.  Host buffers should be
+ * pinned for the copies to be asynchronous.  Same layouts, sizes and errors as
+ * fa_fwd; all ten pointers must be non-null and 16-byte aligned.
+ *
+ * Passes that move 32 MiB or more of input over at least 8 heads are cut into
+ * up to 8 chunks of whole heads (multiples of 4), enqueued round-robin on
+ * three streams the library creates once per device, so the copies of one
+ * chunk overlap the compute of another (the attention of a head does not
+ * depend on the other heads; results are identical to one pass).  That work
+ * is ordered after what the caller enqueued on `stream` before the call, and
+ * `stream` waits for all of it, so work enqueued on `stream` after the call
+ * sees the results.  Enqueueing is serialised per device across threads.
  */
 int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
                   void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,

@@ -96,6 +96,31 @@ def test_hostio_matches_device_path():
     assert torch.equal(oh, want_o) and torch.equal(lh, want_l)
 
 
+@pytest.mark.parametrize("B,H,S,D,dtype,causal", [(1, 64, 4096, 128, "bf16", True),    # 4 chunks on 3 streams
+                                                  (3, 12, 2053, 128, "bf16", False),   # ragged last chunk, odd S
+                                                  (2, 20, 1500, 64, "fp16", True)])
+def test_hostio_chunked_matches_device_path(B, H, S, D, dtype, causal):
+    """Large passes are cut into chunks of heads pipelined over library
+    streams: still bit-identical to one device pass, and ordered before the
+    caller's later work on its stream."""
+    q, k, v = make_qkv(B, H, S, D, dtype, seed=S)
+    want_o, want_l = run_gpu(q, k, v, causal, 0.1)
+    qh, kh, vh = (x.pin_memory() for x in (q, k, v))
+    oh = torch.full_like(qh, float("nan")).pin_memory()
+    lh = torch.full(q.shape[:3], float("nan"), dtype=torch.float32).pin_memory()
+    qd, kd, vd, od = (torch.empty_like(q, device="cuda") for _ in range(4))
+    ld = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        od.fill_(float("nan"))                  # earlier work on the caller's stream
+    fa.fa_fwd_hostio(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, causal=causal, scale=0.1, stream=s)
+    with torch.cuda.stream(s):
+        later = od.to("cpu", non_blocking=False)   # later work on the caller's stream
+    s.synchronize()
+    assert torch.equal(oh, want_o) and torch.equal(lh, want_l)
+    assert torch.equal(later, want_o)
+
+
 def test_rejected_call_launches_nothing():
     q, k, v = (t.cuda() for t in make_qkv(1, 2, 128, 64, "fp16"))
     o = torch.full_like(q, 7.0)
