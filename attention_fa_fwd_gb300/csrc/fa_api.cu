@@ -236,31 +236,57 @@ struct SplitPlan {
     long long units;
 };
 
+// Cost model of the split planner, in SM cycles measured on GB300 for this
+// kernel: one key step of a one-tile unit (softmax, PV and QK strictly in
+// series), one key step of a two-tile unit (the tiles interleave), the fixed
+// part of a unit (Q and first K/V loads, epilogue with the partial's write),
+// and the merge: a fixed part (the second launch, its wait for the attention
+// grid, three dependent L2 round trips; fitted to measured split times) plus
+// its partial bytes read.  Small problems whose one pass is short (the
+// batch-1, 16-head, 1024-token case: 17 us) stay one pass.
+constexpr double kStep1 = 3450.0, kStep2 = 3900.0, kUnitFixed = 5800.0;
+constexpr double kMergeFixed = 20000.0, kMergeBytesPerCycle = 1500.0;
+
+// Split only problems that leave SMs idle, and only when the estimated
+// makespan of the best (tiles per unit, chunk) beats one pass by 10%.
 bool plan_split(int BH, int S, int causal, int num_sms, SplitPlan* sp)
 {
     const int n_qtiles = (S + kBM - 1) / kBM;
     const int tpu1 = ((long long)BH * n_qtiles >= 2ll * num_sms) ? 2 : 1;
-    const long long units1 = (long long)BH * ((n_qtiles + tpu1 - 1) / tpu1);
+    const int ng1 = (n_qtiles + tpu1 - 1) / tpu1;
+    const long long units1 = (long long)BH * ng1;
     if (units1 >= num_sms) return false;
-    const int tpu = n_qtiles >= 2 ? 2 : 1;
-    const int n_qgroups = (n_qtiles + tpu - 1) / tpu;
-    int chunk = 1, uph = 0;
-    for (int c = n_qtiles; c >= 1; --c) {
-        uph = 0;
-        for (int g = 0; g < n_qgroups; ++g) uph += fa::split_chunks(g, tpu, n_qtiles, n_qtiles, causal, c);
-        chunk = c;
-        if ((long long)BH * uph >= num_sms) break;
+    // one pass: one unit per CTA; the longest unit sets the time
+    const double step1 = tpu1 == 2 ? kStep2 : kStep1;
+    const double one_pass = fa::kv_tiles_of(n_qtiles - 1, n_qtiles, causal) * step1 + kUnitFixed;
+    double best = one_pass;
+    bool found = false;
+    for (int tpu = 1; tpu <= (n_qtiles >= 2 ? 2 : 1); ++tpu) {
+        const int n_qgroups = (n_qtiles + tpu - 1) / tpu;
+        for (int c = 1; c < n_qtiles; ++c) {
+            int uph = 0;
+            for (int g = 0; g < n_qgroups; ++g) uph += fa::split_chunks(g, tpu, n_qtiles, n_qtiles, causal, c);
+            const long long units = (long long)BH * uph;
+            const long long rounds = (units + num_sms - 1) / num_sms;
+            const double merge_bytes = (double)units * tpu * kBM * 64 * sizeof(float);   // per 64 columns of D
+            const double cost = rounds * (c * (tpu == 2 ? kStep2 : kStep1) + kUnitFixed) + kMergeFixed +
+                                merge_bytes / kMergeBytesPerCycle;
+            if (cost < best && units < (1ll << 30)) {
+                best = cost;
+                found = true;
+                sp->chunk = c;
+                sp->tpu = tpu;
+                sp->n_qtiles = n_qtiles;
+                sp->n_qgroups = n_qgroups;
+                sp->units_per_head = uph;
+                sp->units = units;
+            }
+        }
     }
-    if (chunk >= n_qtiles) return false;   // every group would be one chunk: nothing to gain
-    sp->chunk = chunk;
-    sp->tpu = tpu;
-    sp->n_qtiles = n_qtiles;
-    sp->n_qgroups = n_qgroups;
-    sp->units_per_head = uph;
-    sp->units = (long long)BH * uph;
-    return true;
+    return found && best < 0.9 * one_pass;
 }
 
+// partial O then partial LSE of every (unit, tile, row)
 size_t split_workspace_bytes(const SplitPlan& sp, int D)
 {
     return (size_t)sp.units * sp.tpu * kBM * (size_t)(D + 1) * sizeof(float);
@@ -402,13 +428,12 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
         m.S = S;
         m.D = D;
         m.n_qtiles = sp->n_qtiles;
-        m.n_kv = sp->n_qtiles;
+        m.n_qgroups = sp->n_qgroups;
         m.tpu = sp->tpu;
         m.causal = causal;
         m.chunk = sp->chunk;
         m.units_per_head = sp->units_per_head;
-        m.bf16 = dtype == FA_DTYPE_BF16;
-        if (fa::launch_merge(m, s) != (int)cudaSuccess) return FA_ERR_CUDA;
+        if (fa::launch_merge(m, dtype == FA_DTYPE_BF16, s) != (int)cudaSuccess) return FA_ERR_CUDA;
     }
     return FA_OK;
 }

@@ -33,7 +33,7 @@ struct Params {
     // Split-KV mode (split_chunk > 0): a unit covers key tiles
     // [chunk * split_chunk, (chunk + 1) * split_chunk) of one query group and
     // writes its O (normalised by its own row sums, fp32) and LSE to the
-    // workspace; fa_merge combines the chunks of each row.
+    // workspace; the merge kernel combines the chunks of each row.
     int split_chunk;            // key tiles per chunk, 0 = no split
     int units_per_head;         // split: sum over query groups of their chunk counts
     float* ws_o;                // split: [n_units][tpu][128][D] fp32
@@ -45,6 +45,17 @@ struct Params {
     int trace_cap;
 };
 
+// Split-KV merge: one block per (batch*head, query tile) combines the tile's
+// chunk partials into O (16-bit) and LSE.
+struct MergeArgs {
+    const float* ws_o;
+    const float* ws_lse;
+    void* o;
+    float* lse;
+    int BH, S, D, n_qtiles, n_qgroups, tpu, causal, chunk, units_per_head;
+};
+int launch_merge(const MergeArgs& a, bool bf16, cudaStream_t s);
+
 // Trace roles and events (FA_TRACE build).  A record is
 // event << 56 | (arg & 0xFFFF) << 40 | (clock64 & (2^40 - 1)).
 enum TraceRole : int { kTrSoftmax0 = 0, kTrSoftmax1 = 1, kTrEpilogue = 2, kTrLoad = 3, kTrMma = 4, kTrKernel = 5,
@@ -55,7 +66,7 @@ enum TraceEvent : unsigned {
     kEvRescale = 3,     // softmax: O rescaled in TMEM (arg j)
     kEvSLoaded = 4,     // softmax: scores in registers (arg j)
     kEvMaxDone = 5,     // softmax: row maximum and re-base decision done (arg j)
-    kEvExpDone = 6,     // softmax: all P stores issued (arg j)
+    kEvExpDone = 6,     // softmax: first half of P published (arg j)
     kEvUnit = 10,       // MMA: unit starts (arg unit index)
     kEvQK = 11,         // MMA: QK issued (arg t << 12 | j)
     kEvPV = 12,         // MMA: PV issued (arg t << 12 | j)
@@ -88,15 +99,6 @@ __host__ __device__ inline int split_chunks(int qg, int tpu, int n_qtiles, int n
     return (kv_tiles_of(last_tile, n_kv, causal) + chunk - 1) / chunk;
 }
 
-// Split-KV merge: combine the chunk partials of every row into O (dtype) and LSE.
-struct MergeArgs {
-    const float* ws_o;
-    const float* ws_lse;
-    void* o;
-    float* lse;
-    int BH, S, D, n_qtiles, n_kv, tpu, causal, chunk, units_per_head, bf16;
-};
-int launch_merge(const MergeArgs& a, cudaStream_t s);
 
 struct LaunchArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;

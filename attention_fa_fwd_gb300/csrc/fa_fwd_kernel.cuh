@@ -79,9 +79,10 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 // Register budget per warpgroup after setmaxnreg: softmax x2, epilogue, control
 // (load + MMA).  The four add up to 512 = 65536 registers / 128 threads; the
-// splits are the spill-free ones ptxas -v reports for each head dim and type.
+// splits are the spill-free ones ptxas -v reports for each head dim and type
+//
 template <int D, bool kBF16, bool kSplit> struct RegSplit {   // split-KV kernels
-    static constexpr uint32_t kSoftmax = 184, kEpilogue = 48, kControl = 96;
+    static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80;
 };
 template <> struct RegSplit<128, false, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80; };
 template <> struct RegSplit<128, true, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80; };
@@ -750,6 +751,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     FA_TRACE_DECL;
     FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvEntry, 0);
+    // split-KV: the merge kernel may be scheduled now (it waits for this grid
+    // to complete before it reads anything)
+    if (kSplit && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {

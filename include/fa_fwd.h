@@ -82,13 +82,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * fa_fwd_splitkv - fa_fwd for problems too small to fill the GPU in one pass.
  *
  * When one pass would give fewer work units than the device has SMs (few
- * heads and short sequences), the key range of every query tile group is cut
- * into chunks of key tiles processed as separate units: each writes the
- * softmax-normalised partial O of its keys (fp32) and their LSE into
- * `workspace`, and a second kernel combines the chunks of every row,
- * O = sum_c exp(LSE_c - LSE) O_c with LSE = ln sum_c exp(LSE_c) - the online
- * softmax merge of "FlashAttention的Triton性能考古学" (核心算法回顾) applied to
- * whole chunks.  Otherwise the call is exactly fa_fwd and ignores `workspace`.
+ * heads and short sequences) and a cost model of the kernel predicts a
+ * shorter run, the key range of every query tile group is cut into chunks of
+ * key tiles processed as separate units: each writes the softmax-normalised
+ * partial O of its keys (fp32) and their LSE into `workspace`, and a second
+ * kernel combines the chunks of every row, O = sum_c exp(LSE_c - LSE) O_c
+ * with LSE = ln sum_c exp(LSE_c) - the online softmax merge of
+ * "FlashAttention的Triton性能考古学" (核心算法回顾) applied to whole chunks.
+ * Otherwise the call is exactly fa_fwd and ignores `workspace`.
  *
  *   workspace        device, caller-owned scratch of at least the size that
  *                    fa_fwd_splitkv_workspace reports, 16-byte aligned; its
@@ -96,8 +97,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   workspace_bytes  its size
  *
  * Two launches (attention, merge) on `stream`; calls that share a workspace
- * must not overlap.  FA_ERR_INVALID_ARG if the workspace is missing or too
- * small while a split is needed; otherwise errors as fa_fwd.
+ * must not overlap.
+ * FA_ERR_INVALID_ARG if the workspace is missing or too small while a split
+ * is needed; otherwise errors as fa_fwd.
  */
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int H, int S, int D, int causal, float scale, int dtype,

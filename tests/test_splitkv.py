@@ -1,6 +1,7 @@
 """Split-KV path (fa_fwd_splitkv): partial results per key chunk in a
-caller-provided workspace, merged by a second kernel.  Parity against the fp64
-oracle, agreement with the one-pass kernel, full row coverage, workspace errors."""
+caller-provided workspace, merged by a second kernel.
+Parity against the fp64 oracle, agreement with the one-pass kernel, full row
+coverage (outputs start as NaN), reuse of a workspace across calls, errors."""
 import pytest
 import torch
 
@@ -22,13 +23,15 @@ def _dt(dtype):
     return torch.bfloat16 if dtype == "bf16" else torch.float16
 
 
-# B, H, S, D, dtype, causal: small problems (one pass fills < 152 SMs)
+# B, H, S, D, dtype, causal: problems with few heads and long keys, where
+# the planner splits (one pass fills < 152 SMs and its longest unit is long)
 CASES = [
-    (1, 16, 1024, 64, "fp16", True),      # the batch-1 long-text workload
     (1, 4, 2048, 128, "bf16", True),
-    (2, 3, 1000, 64, "bf16", False),
-    (1, 1, 4096, 128, "bf16", True),      # one head: one key tile per chunk
-    (1, 2, 300, 128, "fp16", True),       # ragged, few tiles
+    (2, 1, 2000, 64, "fp16", False),      # no mask, ragged
+    (1, 1, 4096, 128, "bf16", True),      # one head, 2-tile chunks
+    (1, 1, 2500, 64, "bf16", True),       # one key tile per chunk, ragged
+    (1, 2, 2047, 64, "fp16", True),       # one query tile per unit
+    (1, 3, 6144, 64, "fp16", True),       # 16-tile chunks
 ]
 
 
@@ -55,6 +58,28 @@ def test_splitkv_parity_and_coverage(B, H, S, D, dtype, causal):
     assert (lse - l1).abs().max().item() <= TOL_LSE
 
 
+def test_workspace_reused_across_calls():
+    # what a call leaves in the workspace must not leak into the next call
+    B, H, S, D = 1, 8, 2048, 128
+    need = fa.splitkv_workspace_bytes(B, H, S, D, True)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    want = None
+    for seed in (5, 6, 5):
+        q, k, v = (x.cuda() for x in make_qkv(B, H, S, D, "bf16", seed=seed))
+        o, lse = fa.fa_fwd_splitkv(q, k, v, causal=True, workspace=ws)
+        assert fa.device_status() == (fa.FA_OK, 0)
+        o1, l1 = fa.fa_fwd(q, k, v, causal=True)
+        torch.cuda.synchronize()
+        assert (o.float() - o1.float()).abs().max().item() <= TOL_O["bf16"]
+        assert (lse - l1).abs().max().item() <= TOL_LSE
+        if seed == 5:
+            if want is None:
+                want = (o.clone(), lse.clone())
+            else:   # the same inputs give the same bits
+                assert torch.equal(o, want[0]) and torch.equal(lse, want[1])
+
+
 def test_no_split_for_large_problems_is_one_pass():
     B, H, S, D = 4, 32, 1024, 128
     assert fa.splitkv_workspace_bytes(B, H, S, D, True) == 0
@@ -65,9 +90,15 @@ def test_no_split_for_large_problems_is_one_pass():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+def test_short_problem_stays_one_pass():
+    # batch 1, 16 heads, 1024 tokens: one pass (17 us) beats split + merge
+    assert fa.splitkv_workspace_bytes(1, 16, 1024, 64, True, torch.float16) == 0
+
+
 def test_workspace_too_small_is_rejected_without_launch():
-    B, H, S, D = 1, 16, 1024, 64
+    B, H, S, D = 1, 4, 2048, 128
     need = fa.splitkv_workspace_bytes(B, H, S, D, True, torch.float16)
+    assert need > 0
     q, k, v = (x.cuda() for x in make_qkv(B, H, S, D, "fp16", seed=1))
     o = torch.full_like(q, 3.0)
     with pytest.raises(fa.FaError) as e:

@@ -31,7 +31,7 @@ def _with_workspace(q, k, v, causal):
 
 
 def test_two_calls_match_the_workspace_entry_point():
-    B, H, S, D = 1, 16, 1024, 64            # takes the split path, ~10 MiB of scratch
+    B, H, S, D = 1, 1, 2500, 64             # takes the split path, ~7 MiB of scratch
     need = fa.splitkv_workspace_bytes(B, H, S, D, True, torch.float16)
     assert 0 < need <= STATIC_SCRATCH_BYTES
     for seed in (1, 2):                     # the second call reuses the array the first filled
@@ -51,13 +51,13 @@ def test_two_calls_match_the_workspace_entry_point():
 
 
 def test_too_large_for_the_static_scratch_is_refused():
-    B, H, S, D = 1, 1, 4096, 128             # split plan of 272 units: ~36 MB of partials
-    need = fa.splitkv_workspace_bytes(B, H, S, D, True, torch.bfloat16)
+    B, H, S, D = 1, 1, 16384, 128            # no mask: split plan of 448 units, ~56 MB of partials
+    need = fa.splitkv_workspace_bytes(B, H, S, D, False, torch.bfloat16)
     assert need > STATIC_SCRATCH_BYTES
     q, k, v = (x.cuda() for x in make_qkv(B, H, S, D, "bf16", seed=3))
     o = torch.full_like(q, 5.0)
     with pytest.raises(fa.FaError) as e:
-        fa.fa_fwd_splitkv_static(q, k, v, causal=True, out=o)
+        fa.fa_fwd_splitkv_static(q, k, v, causal=False, out=o)
     assert e.value.status == fa.FA_ERR_SCRATCH
     torch.cuda.synchronize()
     assert (o == 5.0).all()
