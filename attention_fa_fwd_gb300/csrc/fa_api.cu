@@ -394,6 +394,7 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
         a.grid = (int)(sp->units < num_sms ? sp->units : num_sms);
     }
     a.p.lse = lse;
+    a.p.o = o;
     a.p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.p.timeout_ns = timeout_ns();
     a.p.trace = nullptr;

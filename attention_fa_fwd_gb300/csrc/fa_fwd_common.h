@@ -14,6 +14,7 @@ constexpr int kThreads = 512;  // 4 warpgroups: softmax x2, correction/epilogue,
 // Work-unit schedule and problem constants, identical for every CTA.
 struct Params {
     float* lse;                 // [B*H, S] fp32 output
+    void* o;                    // [B*H, S, D] 16-bit output (stores outside the TMA path)
     unsigned int* status;       // device status word (bounded-wait give-ups)
     unsigned long long timeout_ns;
     int BH;                     // B * H

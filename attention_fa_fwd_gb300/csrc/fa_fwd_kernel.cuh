@@ -74,6 +74,18 @@ __host__ __device__ constexpr float rebase_threshold() { return kBF16 ? 30.0f : 
 #define FA_EXP2_POLY_PAIRS 0
 #endif
 constexpr int kExp2PolyPairs = FA_EXP2_POLY_PAIRS;
+
+// "G6", V44 layout: each softmax warpgroup also runs the epilogue of its own
+// query tile (wait for the last PV, O / l, LSE, 16-bit O stored from
+// registers), and the correction/epilogue warpgroup idles.  Off by default:
+// the separate epilogue is off the critical path here (the MMA issuer waits
+// on it at unit starts only), while in the softmax warpgroups it delays the
+// tile's next unit (the build option exists to measure that).  Split-KV
+// instances keep the separate epilogue.
+#ifndef FA_EPILOGUE_IN_SOFTMAX
+#define FA_EPILOGUE_IN_SOFTMAX 0
+#endif
+constexpr bool kEpilogueInSoftmax = FA_EPILOGUE_IN_SOFTMAX != 0;
 static_assert(kExp2PolyPairs >= 0 && kExp2PolyPairs <= 16, "FA_EXP2_POLY_PAIRS must be in [0, 16]");
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -86,7 +98,7 @@ template <int D, bool kBF16, bool kSplit> struct RegSplit {   // split-KV kernel
 };
 template <> struct RegSplit<128, false, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80; };
 template <> struct RegSplit<128, true, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80; };
-template <> struct RegSplit<64, false, false> { static constexpr uint32_t kSoftmax = 176, kEpilogue = 72, kControl = 88; };
+template <> struct RegSplit<64, false, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72; };
 template <> struct RegSplit<64, true, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72; };
 template <int D, bool kBF16, bool kSplit>
 constexpr bool reg_split_fits()
@@ -275,7 +287,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
     const uint32_t tS = tmem + lane_base + C::col_s(t);
     const uint32_t tO = tmem + lane_base + C::col_o(t);
     const float sl2 = p.scale_log2;
-    uint32_t ph_s = 0, ph_te = 0;
+    uint32_t ph_s = 0, ph_te = 0, ph_o = 0;
     FA_TRACE_DECL;
     const bool tr = (threadIdx.x & 127) == 0;
 
@@ -406,13 +418,47 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), sa, sb);
             l = fmaf(l, h, sa + sb);
         }
-        // hand (l, b) of every row to the epilogue
-        if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarStEmpty + t), ph_te ^ 1u, kSiteSoftmax | (kBarStEmpty + t)))
-            return;
-        ph_te ^= 1u;
-        stats[t * kBM + row] = make_float4(l, b, l + dl, 0.f);
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarStFull + t));
+        if constexpr (kEpilogueInSoftmax && !kSplit) {
+            // this tile's epilogue, here: O_t is final once its last PV completed
+            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarOFull + t), ph_o, kSiteSoftmax | (kBarOFull + t))) return;
+            ph_o ^= 1u;
+            ptx::tc_fence_after();
+            const int qrow = q_tile * kBM + row;
+            const bool in = qrow < p.S;
+            if (in) p.lse[(size_t)un.bh * (size_t)p.S + (size_t)qrow] = (b + ptx::lg2(l)) * kLn2;
+            const float inv_l = 1.0f / (l + dl);
+            const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)un.bh * p.S + qrow) * D);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                ptx::tmem_ld32_wait(tO + c0, o);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float x0, x1;
+                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
+                                   x0, x1);
+                    pk[i] = ptx::pack2<kBF16>(x0, x1);
+                }
+                if (in) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[c0 / 8 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t));
+        } else {
+            // hand (l, b) of every row to the epilogue
+            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarStEmpty + t), ph_te ^ 1u, kSiteSoftmax | (kBarStEmpty + t)))
+                return;
+            ph_te ^= 1u;
+            stats[t * kBM + row] = make_float4(l, b, l + dl, 0.f);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarStFull + t));
+        }
     }
 }
 
@@ -434,6 +480,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
     volatile uint32_t* go = ctl_go;   // leader's wait outcome, read by all 128 threads
     uint32_t ph_o = 0u, ph_t = 0u;   // phase bit of tile t at bit t
     FA_TRACE_DECL;
+    if constexpr (kEpilogueInSoftmax && !kSplit) return;   // the softmax warpgroups run the epilogue
 
     for (int r = 0;; ++r) {
         const Unit un = unit_at<kSplit>(r, p);
