@@ -117,6 +117,8 @@ int launch_d64_f16_split(const LaunchArgs& a, cudaStream_t s);
 int launch_d64_bf16_split(const LaunchArgs& a, cudaStream_t s);
 int launch_d128_f16_split(const LaunchArgs& a, cudaStream_t s);
 int launch_d128_bf16_split(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_f16_dec(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_bf16_dec(const LaunchArgs& a, cudaStream_t s);
 
 // Dynamic shared memory of the instance for head dim D.
 int smem_bytes_for(int D);

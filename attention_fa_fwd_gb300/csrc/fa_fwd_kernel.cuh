@@ -93,22 +93,20 @@ constexpr float kLn2 = 0.693147180559945309f;
 // (load + MMA).  The four add up to 512 = 65536 registers / 128 threads; the
 // splits are the spill-free ones ptxas -v reports for each head dim and type
 //
-template <int D, bool kBF16, bool kSplit> struct RegSplit {   // split-KV kernels
+template <int D, bool kBF16, bool kSplit, bool kDec> struct RegSplit {   // split-KV and decoupled kernels
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80;
 };
-template <> struct RegSplit<128, false, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80; };
-template <> struct RegSplit<128, true, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80; };
-template <> struct RegSplit<64, false, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72; };
-template <> struct RegSplit<64, true, false> { static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72; };
-template <int D, bool kBF16, bool kSplit>
+template <bool kBF16> struct RegSplit<64, kBF16, false, false> {
+    static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72;
+};
+template <int D, bool kBF16, bool kSplit, bool kDec>
 constexpr bool reg_split_fits()
 {
-    using R = RegSplit<D, kBF16, kSplit>;
+    using R = RegSplit<D, kBF16, kSplit, kDec>;
     return 2 * R::kSoftmax + R::kEpilogue + R::kControl == 512;
 }
-static_assert(reg_split_fits<128, false, false>() && reg_split_fits<128, true, false>() &&
-                  reg_split_fits<64, false, false>() && reg_split_fits<64, true, false>() &&
-                  reg_split_fits<128, false, true>() && reg_split_fits<64, true, true>(),
+static_assert(reg_split_fits<128, false, false, false>() && reg_split_fits<64, false, false, false>() &&
+                  reg_split_fits<64, false, false, true>(),
               "register split must add up to 512");
 
 // Barrier indices inside the barrier array.
@@ -123,7 +121,9 @@ enum : int {
     kBarStFull = 14,    // [2] row statistics of tile t in shared memory (4 softmax warps)
     kBarStEmpty = 16,   // [2] epilogue took the statistics (4 epilogue warps)
     kBarDrain = 18,     // MMA drain at exit (commit)
-    kBarKVFull = 19,    // [slots] K or V tile landed (TMA tx)
+    kBarSFree = 19,     // [2] separate-P layout: S_t read into registers (4 softmax warps)
+    kBarPVDone = 21,    // [2] separate-P layout: PV_t finished reading P_t (commit)
+    kBarKVFull = 23,    // [slots] K or V tile landed (TMA tx)
 };
 
 template <int D>
@@ -142,9 +142,21 @@ struct Cfg {
     static constexpr int kOffBars = kOffStats + 2 * kBM * 16;
     static constexpr int kOffCtl = kOffBars + kNumBars * 8;          // [0] TMEM base, [1] abort, [2] epilogue go
     static constexpr int kSmemBytes = kOffCtl + 16 + 1024;            // + slack to align the base to 1 KB
-    // TMEM columns of the score region S_t and the output accumulator O_t
+    // TMEM columns of the score region S_t, the output accumulator O_t and P_t.
+    // D=128 fills the 512 columns with S0 | S1 | O0 | O1, so P_t overwrites the
+    // first half of S_t and the next QK_t must wait for PV_t.  D=64 leaves 128
+    // columns free: the decoupled instances (kDec, launched for one query tile
+    // per unit) give P_t its own 64 there, so QK_t(j+1) can run as soon as the
+    // softmax has read S_t(j), while P_t(j) waits for its PV.  With two tiles
+    // per unit P_t stays on S_t: the tiles alternate anyway, and P in the free
+    // columns measured 7% slower there.
+    static constexpr bool kSepP = (D == 64);
     __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
     __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
+    __device__ static constexpr uint32_t col_p(int t, bool decoupled)
+    {
+        return (kSepP && decoupled) ? 384u + (t ? 64u : 0u) : col_s(t);
+    }
 };
 
 struct Unit {
@@ -275,7 +287,7 @@ enum : uint32_t { kSiteSoftmax = 0x100, kSiteEpilogue = 0x300, kSiteLoad = 0x400
 
 // ---------------------------------------------------------------------------------
 // Softmax warpgroup t: one thread per query row of tile t.
-template <int D, bool kBF16, bool kSplit>
+template <int D, bool kBF16, bool kSplit, bool kDec>
 __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx& wc, int t, uint32_t tmem,
                                              uint32_t bars, float4* stats)
 {
@@ -286,8 +298,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::col_s(t);
     const uint32_t tO = tmem + lane_base + C::col_o(t);
+    // decoupled order (separate P): the next QK_t runs before PV_t, so P_t and
+    // O_t wait for that PV explicitly; in the shared order S_t(j) implies that
+    // PV_t(j-1) has finished
+    static_assert(!kDec || C::kSepP, "the decoupled order needs P in its own columns");
+    const uint32_t tP = tmem + lane_base + C::col_p(t, kDec);
     const float sl2 = p.scale_log2;
     uint32_t ph_s = 0, ph_te = 0, ph_o = 0;
+    uint32_t n_pub = 0;   // separate P: P tiles this warpgroup published (one PV each)
     FA_TRACE_DECL;
     const bool tr = (threadIdx.x & 127) == 0;
 
@@ -323,6 +341,12 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             ptx::tmem_wait_ld();
             ptx::reg_fence(sr);
             ptx::reg_fence(pm);
+            if constexpr (kDec) {
+                // S_t is in registers: the MMA issuer may compute the next S_t now
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarSFree + t));
+            }
             FA_TRACE_EV(tr, t, kEvSLoaded, j);
             float* s = reinterpret_cast<float*>(sr);
             float mraw;
@@ -363,6 +387,15 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 b = cand;
             }
             FA_TRACE_EV(tr, t, kEvMaxDone, j);
+            if constexpr (kDec) {
+                // P_t and O_t are free once the PV of the previously published P_t
+                // completed (in this order S_t(j) does not imply it)
+                if (n_pub > 0 && !ptx::mbar_wait_warp(wc, bars + 8 * (kBarPVDone + t), (n_pub - 1) & 1u,
+                                                      kSiteSoftmax | (kBarPVDone + t)))
+                    return;
+                ++n_pub;
+                ptx::tc_fence_after();
+            }
             if (rescale) {
                 // this warp's 32 rows of O_t are scaled by 2^(b_old - b_new)
 #pragma unroll 1
@@ -403,7 +436,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                     acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
                     pk[i] = ptx::pack2<kBF16>(p0, p1);
                 }
-                ptx::tmem_st16(tS + c * 16, pk);
+                ptx::tmem_st16(tP + c * 16, pk);
                 if (c == 1 || c == 3) {
                     // publish P (and, at c == 1, the rescaled O) for the MMA issuer
                     ptx::tmem_wait_st();
@@ -649,14 +682,14 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
 
 // ---------------------------------------------------------------------------------
 // tcgen05 MMA issuer (one thread).
-template <int D, bool kBF16, bool kSplit>
+template <int D, bool kBF16, bool kSplit, bool kDec>
 __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem, uint32_t smem_base,
                                          uint32_t bars)
 {
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);   // Q, K both K-major
     constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, kBF16, true);      // V is MN-major (D contiguous)
-    uint32_t ph_q = 0u, ph_ph = 0u, ph_p = 0u, ph_oe = 0u;   // phase bit of tile t at bit t
+    uint32_t ph_q = 0u, ph_ph = 0u, ph_p = 0u, ph_oe = 0u, ph_sf = 0u;   // phase bit of tile t at bit t
     uint32_t kv_count = 0;
     FA_TRACE_DECL;
 
@@ -693,7 +726,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = half * 4 + k4;
-            ptx::mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+            ptx::mma_ts(tmem + C::col_o(t), tmem + C::col_p(t, kDec) + kk * 8,
                         ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
     };
@@ -710,6 +743,12 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             if (un.nkv[t] == 0) continue;
             if (!ptx::mbar_wait(wc, bars + 8 * (kBarQFull + t), (ph_q >> t) & 1u, kSiteMma | (kBarQFull + t))) goto done;
             ph_q ^= 1u << t;
+            if constexpr (kDec) {
+                // S_t is overwritten: the softmax must have read the previous one
+                if (!ptx::mbar_wait(wc, bars + 8 * (kBarSFree + t), ((ph_sf >> t) & 1u) ^ 1u, kSiteMma | (kBarSFree + t)))
+                    goto done;
+                ph_sf ^= 1u << t;
+            }
         }
         if (!kv_wait(kvb)) goto done;
         ptx::tc_fence_after();
@@ -725,6 +764,29 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         for (int j = un.j0; j < un.nmax; ++j) {
             const uint32_t iv = kvb + 2 * (j - un.j0) + 1, ik = iv + 1;
             bool v_ready = false, k_ready = false;
+            if constexpr (kDec) {
+                // the next scores first: QK_t(j+1) needs only S_t(j) read into the
+                // softmax's registers, so it runs while that softmax computes P_t(j)
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (j + 1 < un.nkv[t]) {
+                        if (!ptx::mbar_wait(wc, bars + 8 * (kBarSFree + t), ((ph_sf >> t) & 1u) ^ 1u,
+                                            kSiteMma | (kBarSFree + t)))
+                            goto done;
+                        ph_sf ^= 1u << t;
+                        if (!k_ready) {
+                            if (!kv_wait(ik)) goto done;
+                            k_ready = true;
+                        }
+                        ptx::tc_fence_after();
+                        FA_TRACE_EV(true, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
+                        issue_qk(t, ik);
+                        ptx::mma_commit(bars + 8 * (kBarSFull + t));
+                        FA_TRACE_EV(true, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
+                        if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
+                    }
+                }
+            }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (j < un.nkv[t]) {
@@ -753,19 +815,22 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     ptx::tc_fence_after();
                     issue_pv(t, iv, 1, true);
                     FA_TRACE_EV(true, kTrMma, kEvPV, ((uint32_t)t << 12) | j);
+                    if constexpr (kDec) ptx::mma_commit(bars + 8 * (kBarPVDone + t));   // P_t may be rewritten
                     if (j == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarOFull + t));
                 }
-                if (j + 1 < un.nkv[t]) {
-                    if (!k_ready) {
-                        if (!kv_wait(ik)) goto done;
-                        k_ready = true;
-                        ptx::tc_fence_after();
+                if constexpr (!kDec) {
+                    if (j + 1 < un.nkv[t]) {
+                        if (!k_ready) {
+                            if (!kv_wait(ik)) goto done;
+                            k_ready = true;
+                            ptx::tc_fence_after();
+                        }
+                        FA_TRACE_EV(true, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
+                        issue_qk(t, ik);
+                        ptx::mma_commit(bars + 8 * (kBarSFull + t));
+                        FA_TRACE_EV(true, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
+                        if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
                     }
-                    FA_TRACE_EV(true, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
-                    issue_qk(t, ik);
-                    ptx::mma_commit(bars + 8 * (kBarSFull + t));
-                    FA_TRACE_EV(true, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
-                    if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
                 }
             }
             if (j + 1 < un.nmax) kv_release(ik);
@@ -780,7 +845,7 @@ done:
 }
 
 // ---------------------------------------------------------------------------------
-template <int D, bool kBF16, bool kSplit>
+template <int D, bool kBF16, bool kSplit, bool kDec>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -813,6 +878,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars + 8 * (kBarOEmpty + t), 4);
             ptx::mbar_init(bars + 8 * (kBarStFull + t), 4);
             ptx::mbar_init(bars + 8 * (kBarStEmpty + t), 4);
+            ptx::mbar_init(bars + 8 * (kBarSFree + t), 4);
+            ptx::mbar_init(bars + 8 * (kBarPVDone + t), 1);
         }
         ptx::mbar_init(bars + 8 * kBarDrain, 1);
         for (int s = 0; s < C::kSlots; ++s) {
@@ -840,17 +907,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvSetup, 0);
 
     if (warp < 8) {
-        ptx::setmaxnreg_inc<RegSplit<D, kBF16, kSplit>::kSoftmax>();
-        softmax_role<D, kBF16, kSplit>(p, wc, warp >> 2, tmem, bars, stats);
+        ptx::setmaxnreg_inc<RegSplit<D, kBF16, kSplit, kDec>::kSoftmax>();
+        softmax_role<D, kBF16, kSplit, kDec>(p, wc, warp >> 2, tmem, bars, stats);
     } else if (warp < 12) {
-        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit>::kEpilogue>();
+        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kEpilogue>();
         correction_epilogue_role<D, kBF16, kSplit>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
     } else {
-        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit>::kControl>();
+        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kControl>();
         if (warp == 12) {
             if (lane == 0) load_role<D, kSplit>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {
-            if (lane == 0) mma_role<D, kBF16, kSplit>(p, wc, tmem, base, bars);
+            if (lane == 0) mma_role<D, kBF16, kSplit, kDec>(p, wc, tmem, base, bars);
         }
         __syncwarp();
     }
@@ -864,10 +931,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool kBF16, bool kSplit>
+template <int D, bool kBF16, bool kSplit, bool kDec = false>
 int launch_instance(const LaunchArgs& a, cudaStream_t stream)
 {
-    auto kern = fa_fwd_kernel<D, kBF16, kSplit>;
+    auto kern = fa_fwd_kernel<D, kBF16, kSplit, kDec>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
     if (e != cudaSuccess) return (int)e;
     cudaLaunchConfig_t cfg = {};

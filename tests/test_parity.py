@@ -38,11 +38,29 @@ def test_shapes(B, H, S, D, dtype, causal):
     check_full(B, H, S, D, dtype, causal, seed=B * 1000 + S)
 
 
+def _tiles_per_unit(B, H, S, D, causal):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return fa.plan(B, H, S, D, causal, sms)["tiles_per_unit"]
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_many_heads_two_tiles_per_unit(causal):
     # enough query tiles that units hold two tiles (ping-pong path), odd tile count
-    check_full(2, 80, 384, 64, "fp16", causal, seed=5)
-    check_full(1, 160, 300, 128, "bf16", causal, seed=6)
+    for (B, H, S, D, dtype, seed) in [(2, 80, 384, 64, "fp16", 5), (1, 100, 400, 64, "bf16", 7),
+                                      (1, 160, 300, 128, "bf16", 6)]:
+        assert _tiles_per_unit(B, H, S, D, causal) == 2
+        check_full(B, H, S, D, dtype, causal, seed=seed)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_64_one_tile_per_unit(dtype, causal):
+    # one query tile per unit: at D=64 this is the decoupled order (P in its
+    # own TMEM columns, the next QK issued before the PV); several key tiles
+    # and a ragged tail so the S-free / PV-done hand-offs cycle many times
+    for (B, H, S, seed) in [(1, 4, 1100, 11), (2, 3, 777, 12)]:
+        assert _tiles_per_unit(B, H, S, 64, causal) == 1
+        check_full(B, H, S, 64, dtype, causal, seed=seed)
 
 
 def test_batch1_causal_workload_full():
