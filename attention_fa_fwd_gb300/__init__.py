@@ -170,8 +170,8 @@ def fa_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bo
     if lse is None:
         lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
     with torch.cuda.device(q.device):
-        need = splitkv_workspace_bytes(B, H, S, D, causal, q.dtype)
         if workspace is None:
+            need = splitkv_workspace_bytes(B, H, S, D, causal, q.dtype)
             workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
         ws_bytes = workspace.numel() * workspace.element_size()
         rc = lib().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),

@@ -33,6 +33,7 @@ int g_trace_ctas = 0, g_trace_cap = 0;
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_num_sms[kMaxDevices];     // 0 = not queried yet
 std::atomic<int> g_cc[kMaxDevices];          // major*10 + minor, 0 = not queried yet
+std::atomic<void*> g_status_addr[kMaxDevices];   // device address of g_fa_status, nullptr = not looked up
 
 unsigned long long timeout_ns()
 {
@@ -249,7 +250,7 @@ constexpr double kMergeFixed = 20000.0, kMergeBytesPerCycle = 1500.0;
 
 // Split only problems that leave SMs idle, and only when the estimated
 // makespan of the best (tiles per unit, chunk) beats one pass by 10%.
-bool plan_split(int BH, int S, int causal, int num_sms, SplitPlan* sp)
+bool plan_split_search(int BH, int S, int causal, int num_sms, SplitPlan* sp)
 {
     const int n_qtiles = (S + kBM - 1) / kBM;
     const int tpu1 = ((long long)BH * n_qtiles >= 2ll * num_sms) ? 2 : 1;
@@ -286,6 +287,44 @@ bool plan_split(int BH, int S, int causal, int num_sms, SplitPlan* sp)
     return found && best < 0.9 * one_pass;
 }
 
+// The search walks every (tiles per unit, chunk) over every query group, which
+// is O(n_qtiles^2): tens of microseconds of host time for long rows, more than
+// the kernels of a small problem take.  Callers repeat shapes (the workspace
+// query, then the call; every step of a loop), so recent answers are kept.
+struct SplitMemo {
+    int BH, S, causal, num_sms;
+    bool found;
+    SplitPlan sp;
+};
+constexpr int kSplitMemo = 16;
+std::mutex g_split_mu;
+SplitMemo g_split_memo[kSplitMemo];
+int g_split_n = 0, g_split_next = 0;
+
+bool plan_split(int BH, int S, int causal, int num_sms, SplitPlan* sp)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_split_mu);
+        for (int i = 0; i < g_split_n; ++i) {
+            const SplitMemo& m = g_split_memo[i];
+            if (m.BH == BH && m.S == S && m.causal == causal && m.num_sms == num_sms) {
+                if (m.found) *sp = m.sp;
+                return m.found;
+            }
+        }
+    }
+    SplitMemo m{BH, S, causal, num_sms, false, SplitPlan{}};
+    m.found = plan_split_search(BH, S, causal, num_sms, &m.sp);
+    {
+        std::lock_guard<std::mutex> lk(g_split_mu);
+        g_split_memo[g_split_next] = m;
+        g_split_next = (g_split_next + 1) % kSplitMemo;
+        if (g_split_n < kSplitMemo) ++g_split_n;
+    }
+    if (m.found) *sp = m.sp;
+    return m.found;
+}
+
 // partial O then partial LSE of every (unit, tile, row)
 size_t split_workspace_bytes(const SplitPlan& sp, int D)
 {
@@ -312,6 +351,38 @@ int make_tmap(CUtensorMap* m, const void* ptr, int BH, int S, int D, int dtype)
 
 namespace fa {
 int smem_bytes_for(int D) { return D == 64 ? Cfg<64>::kSmemBytes : Cfg<128>::kSmemBytes; }
+
+namespace {
+// (kernel, devices with the opt-in set) for the few kernel instances there are
+constexpr int kOptInSlots = 32;
+std::mutex g_opt_in_mu;
+const void* g_opt_in_kern[kOptInSlots];
+unsigned long long g_opt_in_devs[kOptInSlots];
+int g_opt_in_n = 0;
+}  // namespace
+
+bool smem_opt_in_done(const void* kern, int device)
+{
+    std::lock_guard<std::mutex> lk(g_opt_in_mu);
+    for (int i = 0; i < g_opt_in_n; ++i)
+        if (g_opt_in_kern[i] == kern) return (g_opt_in_devs[i] >> (device & 63)) & 1ull;
+    return false;
+}
+
+void smem_opt_in_mark(const void* kern, int device)
+{
+    std::lock_guard<std::mutex> lk(g_opt_in_mu);
+    for (int i = 0; i < g_opt_in_n; ++i)
+        if (g_opt_in_kern[i] == kern) {
+            g_opt_in_devs[i] |= 1ull << (device & 63);
+            return;
+        }
+    if (g_opt_in_n < kOptInSlots) {   // a full table only means the opt-in is set again on every launch
+        g_opt_in_kern[g_opt_in_n] = kern;
+        g_opt_in_devs[g_opt_in_n] = 1ull << (device & 63);
+        ++g_opt_in_n;
+    }
+}
 }  // namespace fa
 
 extern "C" {
@@ -377,10 +448,10 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
             float scale, int dtype, int num_sms, const SplitPlan* sp, float* ws, void* stream)
 {
     fa::LaunchArgs a;
-    plan(B, H, S, D, causal, num_sms, nullptr, &a.p);
     fa_launch_info_t info;
-    plan(B, H, S, D, causal, num_sms, &info, nullptr);
+    plan(B, H, S, D, causal, num_sms, &info, &a.p);
     a.grid = info.grid;
+    if (cudaGetDevice(&a.device) != cudaSuccess || a.device < 0 || a.device >= kMaxDevices) return FA_ERR_CUDA;
     const int BH = B * H;
     if (sp) {
         a.p.tpu = sp->tpu;
@@ -405,8 +476,11 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
     a.p.trace_ctas = g_trace_ctas;
     a.p.trace_cap = g_trace_cap;
 #endif
-    void* status = nullptr;
-    if (cudaGetSymbolAddress(&status, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+    void* status = g_status_addr[a.device].load(std::memory_order_acquire);
+    if (!status) {
+        if (cudaGetSymbolAddress(&status, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+        g_status_addr[a.device].store(status, std::memory_order_release);
+    }
     a.p.status = static_cast<unsigned int*>(status);
     if (make_tmap(&a.tm_q, q, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_k, k, BH, S, D, dtype) != FA_OK ||
         make_tmap(&a.tm_v, v, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_o, o, BH, S, D, dtype) != FA_OK)

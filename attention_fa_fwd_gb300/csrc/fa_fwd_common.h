@@ -105,6 +105,7 @@ struct LaunchArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;
     Params p;
     int grid;
+    int device;   // current CUDA device (0..63): the launcher sets per-device kernel attributes once
 };
 
 // One launcher per (head dim, dtype) instance; each lives in its own
@@ -119,9 +120,17 @@ int launch_d128_f16_split(const LaunchArgs& a, cudaStream_t s);
 int launch_d128_bf16_split(const LaunchArgs& a, cudaStream_t s);
 int launch_d64_f16_dec(const LaunchArgs& a, cudaStream_t s);
 int launch_d64_bf16_dec(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_f16_split_dec(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_bf16_split_dec(const LaunchArgs& a, cudaStream_t s);
 
 // Dynamic shared memory of the instance for head dim D.
 int smem_bytes_for(int D);
+
+// Whether the large shared-memory opt-in of kernel `kern` is already set on
+// `device`, and recording that it is.  Keyed by the kernel's own address, so
+// several builds of this library loaded into one process never share an entry.
+bool smem_opt_in_done(const void* kern, int device);
+void smem_opt_in_mark(const void* kern, int device);
 
 // Kernel that waits on a barrier nobody arrives on (bounded-wait self-test).
 int launch_wait_selftest(unsigned int* status, unsigned long long timeout_ns, cudaStream_t s);

@@ -935,8 +935,14 @@ template <int D, bool kBF16, bool kSplit, bool kDec = false>
 int launch_instance(const LaunchArgs& a, cudaStream_t stream)
 {
     auto kern = fa_fwd_kernel<D, kBF16, kSplit, kDec>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
-    if (e != cudaSuccess) return (int)e;
+    // the shared-memory opt-in is a per-device property of the kernel: set it
+    // on the first launch on each device only (it costs a driver call)
+    cudaError_t e = cudaSuccess;
+    if (!smem_opt_in_done(reinterpret_cast<const void*>(kern), a.device)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+        if (e != cudaSuccess) return (int)e;
+        smem_opt_in_mark(reinterpret_cast<const void*>(kern), a.device);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);

@@ -105,3 +105,32 @@ def test_plan_rejects_what_fa_fwd_rejects(L):
         fa.plan(1, 2, 128, 96, 0, 152)
     with pytest.raises(fa.FaError):
         fa.plan(1, 2, 128, 64, 0, 0)
+
+
+def _defined_unique_symbols(path):
+    """Names of the defined STB_GNU_UNIQUE symbols in an ELF64 little-endian
+    shared object's dynamic symbol table."""
+    import struct
+    data = open(path, "rb").read()
+    assert data[:4] == b"\x7fELF" and data[4] == 2 and data[5] == 1, "expected ELF64 little-endian"
+    shoff, = struct.unpack_from("<Q", data, 0x28)
+    shentsize, shnum = struct.unpack_from("<HH", data, 0x3A)
+    sections = [struct.unpack_from("<IIQQQQIIQQ", data, shoff + i * shentsize) for i in range(shnum)]
+    names = []
+    for (_, sh_type, _, _, off, size, link, _, _, entsize) in sections:
+        if sh_type != 11:   # SHT_DYNSYM
+            continue
+        str_off = sections[link][4]
+        for j in range(size // entsize):
+            st_name, st_info, _, st_shndx = struct.unpack_from("<IBBH", data, off + j * entsize)
+            if st_info >> 4 == 10 and st_shndx != 0:   # STB_GNU_UNIQUE, defined here
+                end = data.index(b"\0", str_off + st_name)
+                names.append(data[str_off + st_name:end].decode())
+    return names
+
+
+def test_library_has_no_process_wide_unique_objects(L):
+    # several builds of the library (option builds, trace build) may be loaded
+    # into one process; a GNU-unique object would be shared between all of
+    # them (per-kernel state of one build applied to another's kernels)
+    assert _defined_unique_symbols(L._name) == []
