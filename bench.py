@@ -199,6 +199,35 @@ def time_oracle(w, q, k, v, budget_s: float, steps: int, seed: int = 0):
     return statistics.median(tflops), statistics.median(per_step), desc, nthreads
 
 
+# the kernel's re-base thresholds (log2 units) by input type
+KERNEL_REBASE_T = {"bf16": 30.0, "fp16": 15.0}
+
+
+def rescale_events(w, q, k, v, heads: int = 1):
+    """Re-bases counted by the oracle's lazy-rescale recurrence (row level, P
+    rounded to the input type) on the first `heads` heads at full length, for
+    the pages' threshold 8 and the kernel's, run side by side."""
+    import oracle
+    from fa_inputs import to_f64
+    BH, S, D = w.B * w.H, w.S, w.D
+    qs, ks, vs = (to_f64(x.reshape(BH, S, D)[:heads].unsqueeze(0)) for x in (q, k, v))
+    out = {}
+
+    def run(t):
+        out[t] = oracle.attention_lazy(qs, ks, vs, w.causal, w.scale, 128, t, w.dtype, nthreads=heads)[2]
+
+    ts = [8.0, KERNEL_REBASE_T[w.dtype]]
+    th = [threading.Thread(target=run, args=(t,)) for t in ts]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    steps = out[ts[0]]["steps"]
+    return {"model": "oracle lazy-rescale recurrence, row level", "heads": heads, "row_tile_steps": steps,
+            "row_rebases": {f"T={t:g}": out[t]["rebases"] for t in ts},
+            "kernel_T": KERNEL_REBASE_T[w.dtype]}
+
+
 def aggregate(ms_local: float, flops_per_rank: float, world: int, dist=None, device=None):
     """Max of the ranks' timed milliseconds and the whole-job TFLOPS over it
     (every rank ran `flops_per_rank`).  `dist` is torch.distributed or None."""
@@ -278,6 +307,15 @@ def run_ours(args, w):
     barrier()
     clocks = sampler.stop()
     ms = ev0.elapsed_time(ev1)
+    # best single step: a short loop of individually timed launches
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(min(50, args.steps))]
+    for a, b in pairs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_best = min(a.elapsed_time(b) for a, b in pairs)
     status, site = fa.device_status(clear=True, stream=stream)
     if status != fa.FA_OK:
         raise SystemExit(f"in-kernel wait gave up at site {site:#x}")
@@ -329,6 +367,7 @@ def run_ours(args, w):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "ms_per_step_best": round(ms_best, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "fp16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
@@ -352,6 +391,8 @@ def run_ours(args, w):
                                 "kind": "oracle", "sample": desc}
     elif not args.no_cpu_baseline:
         line["cpu_baseline"] = None
+    if w.kind == "stress" and not args.no_cpu_baseline:
+        line["rescale"] = rescale_events(w, q, k, v)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
