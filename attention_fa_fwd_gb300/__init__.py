@@ -68,12 +68,15 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp] + dims
         L.fa_fwd_launch_info.argtypes = [i, i, i, i, i, i, ctypes.POINTER(LaunchInfo)]
         L.fa_fwd_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(LaunchInfo)]
+        us = ctypes.POINTER(ctypes.c_ushort)
+        L.fa_fwd_schedule_table.argtypes = [i, i, i, i, i, i, i, us, i, us, i, ctypes.POINTER(i),
+                                            ctypes.POINTER(i)]
         L.fa_device_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint)]
         L.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
         L.fa_selftest_exp2_poly.argtypes = [vp, vp, i, vp]
         L.fa_strerror.argtypes = [i]
         L.fa_strerror.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_hostio", "fa_fwd_launch_info", "fa_fwd_plan",
+        for name in ("fa_fwd", "fa_fwd_hostio", "fa_fwd_launch_info", "fa_fwd_plan", "fa_fwd_schedule_table",
                      "fa_device_status", "fa_selftest_wait_timeout", "fa_selftest_exp2_poly", "fa_fwd_splitkv",
                      "fa_fwd_splitkv_workspace", "fa_fwd_splitkv_static"):
             getattr(L, name).restype = i
@@ -248,6 +251,23 @@ def plan(B: int, H: int, S: int, D: int, causal: bool, num_sms: int, dtype=torch
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_plan")
     return info.as_dict()
+
+
+def schedule_table(B: int, H: int, S: int, D: int, causal: bool, num_sms: int, dtype=torch.bfloat16):
+    """Per-CTA unit lists of the host list schedule (pure host computation):
+    a list of `grid` lists of unit indices, or None when the launch uses a
+    closed-form schedule."""
+    cap = 1 << 16
+    off = (ctypes.c_ushort * (cap + 1))()
+    units = (ctypes.c_ushort * cap)()
+    n_ctas, n_units = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().fa_fwd_schedule_table(B, H, S, D, int(bool(causal)), _DTYPE.get(dtype, 99), num_sms, off, cap + 1,
+                                     units, cap, ctypes.byref(n_ctas), ctypes.byref(n_units))
+    if rc == FA_ERR_UNSUPPORTED:
+        return None
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_schedule_table")
+    return [list(units[off[c]:off[c + 1]]) for c in range(n_ctas.value)]
 
 
 def device_status(clear: bool = True, stream=None) -> tuple[int, int]:

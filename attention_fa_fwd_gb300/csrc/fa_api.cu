@@ -167,6 +167,121 @@ int plan_head_group(int BH, int S, int D, int n_qtiles, int tpu, int n_qgroups, 
     return pick;
 }
 
+// ---- table schedule ----------------------------------------------------------
+// For causal launches of several rounds that fit the table, the host computes a
+// list schedule instead of a closed form: the units, ordered group by group
+// (head_group heads at a time, so the heads in flight share L2) and longest
+// first inside a group, go one at a time to the CTA with the least modelled work
+// so far (a unit costs its key tiles plus two for its fixed part).  That is
+// longest-processing-time list scheduling per group.  Its balance moves with the
+// group size, so the planner replays it for every group whose K/V fits
+// kTableKVBudget and keeps the smallest group within 0.5% of the best.  It
+// balances the causal triangle where mirror pairs leave rounds half-empty and a
+// snake needs all heads in one group (modelled, most loaded CTA over the mean:
+// 4x32x4096 1.04 pairs, 1.008 here with 8-head groups; 8x16x2048 1.19 pairs,
+// 1.026 here).  Tables are cached per shape; each launch carries its copy in the
+// kernel parameters.
+constexpr long long kTableKVBudget = 64ll << 20;   // bytes of K/V per group of heads
+
+struct SchedTable {
+    int BH, S, D, tpu, causal, grid, hg;
+    std::vector<unsigned short> off, unit;
+};
+
+// Assigns the units (heads in groups of hg) to `grid` CTAs; returns the most
+// loaded CTA's modelled work over the mean, and the per-CTA lists if `per`.
+double list_schedule(int BH, int n_qtiles, int tpu, int causal, int grid, int hg,
+                     std::vector<std::vector<unsigned short>>* per)
+{
+    const int n_qgroups = (n_qtiles + tpu - 1) / tpu;
+    auto cost = [&](int qg) {
+        int last = qg * tpu + tpu - 1;
+        if (last > n_qtiles - 1) last = n_qtiles - 1;
+        return (double)fa::kv_tiles_of(last, n_qtiles, causal) + 2.0;
+    };
+    if (per) per->assign((size_t)grid, {});
+    // min-heap of (load, cta), ties to the lower CTA
+    std::vector<std::pair<double, int>> heap;
+    heap.reserve((size_t)grid);
+    for (int c = 0; c < grid; ++c) heap.push_back({0.0, c});
+    auto later = [](const std::pair<double, int>& a, const std::pair<double, int>& b) {
+        return a.first > b.first || (a.first == b.first && a.second > b.second);
+    };
+    std::make_heap(heap.begin(), heap.end(), later);
+    double total = 0.0;
+    for (int h0 = 0; h0 < BH; h0 += hg) {
+        const int h1 = std::min(BH, h0 + hg);
+        for (int rank = 0; rank < n_qgroups; ++rank) {
+            const int qg = causal ? n_qgroups - 1 - rank : rank;
+            const double w = cost(qg);
+            for (int h = h0; h < h1; ++h) {
+                std::pop_heap(heap.begin(), heap.end(), later);
+                if (per) (*per)[(size_t)heap.back().second].push_back((unsigned short)(h * n_qgroups + qg));
+                heap.back().first += w;
+                total += w;
+                std::push_heap(heap.begin(), heap.end(), later);
+            }
+        }
+    }
+    double mx = 0.0;
+    for (const auto& e : heap) mx = std::max(mx, e.first);
+    return mx / (total / grid);
+}
+
+bool table_applies(int causal, long long units, int grid)
+{
+    return causal && units > grid && units <= fa::kSchedTableMaxUnits && grid <= fa::kSchedTableMaxCtas;
+}
+
+// The table for this shape (built and cached on first use); copies it into *p
+// when p is not null and returns its head group.
+int table_plan(int BH, int S, int D, int n_qtiles, int tpu, int causal, int grid, fa::Params* p)
+{
+    static std::mutex mu;
+    static std::vector<SchedTable> cache;   // recent shapes
+    std::lock_guard<std::mutex> lock(mu);
+    const SchedTable* t = nullptr;
+    for (const SchedTable& e : cache)
+        if (e.BH == BH && e.S == S && e.D == D && e.tpu == tpu && e.causal == causal && e.grid == grid) {
+            t = &e;
+            break;
+        }
+    if (!t) {
+        const long long kv_head_bytes = 2ll * S * D * 2;
+        long long cap = kTableKVBudget / kv_head_bytes;
+        cap = std::max(1ll, std::min(cap, (long long)BH));
+        std::vector<double> score((size_t)cap + 1, 0.0);
+        double best = 1e30;
+        for (int hg = 1; hg <= cap; ++hg) {
+            score[(size_t)hg] = list_schedule(BH, n_qtiles, tpu, causal, grid, hg, nullptr);
+            best = std::min(best, score[(size_t)hg]);
+        }
+        int pick = (int)cap;
+        for (int hg = 1; hg <= cap; ++hg)
+            if (score[(size_t)hg] <= best + 0.005) {
+                pick = hg;
+                break;
+            }
+        SchedTable n{BH, S, D, tpu, causal, grid, pick, {}, {}};
+        std::vector<std::vector<unsigned short>> per;
+        list_schedule(BH, n_qtiles, tpu, causal, grid, pick, &per);
+        n.off.assign((size_t)grid + 1, 0);
+        for (int c = 0; c < grid; ++c) {
+            n.off[(size_t)c] = (unsigned short)n.unit.size();
+            n.unit.insert(n.unit.end(), per[(size_t)c].begin(), per[(size_t)c].end());
+        }
+        n.off[(size_t)grid] = (unsigned short)n.unit.size();
+        if (cache.size() >= 16) cache.erase(cache.begin());
+        cache.push_back(std::move(n));
+        t = &cache.back();
+    }
+    if (p) {
+        std::copy(t->off.begin(), t->off.end(), p->tab_off);
+        std::copy(t->unit.begin(), t->unit.end(), p->tab_unit);
+    }
+    return t->hg;
+}
+
 // Work-unit geometry (see the schedule comment in fa_fwd_kernel.cuh).
 void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t* info, fa::Params* p)
 {
@@ -186,10 +301,15 @@ void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t*
     // power cap).  Then the mirror-pair schedule is used instead: slightly worse
     // balance, but a CTA's two units share one head and a round covers few heads.
     // With a single round every CTA takes one unit.  Without the mask every unit
-    // costs the same and heads simply go in order.
+    // costs the same and heads simply go in order.  Causal launches of several
+    // rounds that fit the parameter table take the host's list schedule instead
+    // (see table_plan), which gets both balance and locality.
     int head_group = 1;
     bool pairs = false;
-    if (causal && units > grid) {
+    const bool table = table_applies(causal, units, grid);
+    if (table) {
+        head_group = table_plan(BH, S, D, n_qtiles, tpu, causal, grid, p);
+    } else if (causal && units > grid) {
         head_group = plan_head_group(BH, S, D, n_qtiles, tpu, n_qgroups, units, grid);
         pairs = grid < 4 * head_group;
     } else if (causal) {
@@ -204,7 +324,7 @@ void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t*
         info->units = (int)units;
         info->head_group = head_group;
         info->num_sms = num_sms;
-        info->schedule = pairs ? 1 : 0;
+        info->schedule = table ? 2 : (pairs ? 1 : 0);
     }
     if (p) {
         p->BH = BH;
@@ -214,7 +334,7 @@ void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t*
         p->tpu = tpu;
         p->n_qgroups = n_qgroups;
         p->n_units = (int)units;
-        p->sched = pairs ? fa::kSchedPairs : fa::kSchedSnake;
+        p->sched = table ? fa::kSchedTable : (pairs ? fa::kSchedPairs : fa::kSchedSnake);
         p->head_group = head_group;
         p->pairs_per_head = pairs_per_head;
         p->n_pairs = (long long)BH * pairs_per_head;
@@ -419,6 +539,27 @@ int fa_fwd_plan(int B, int H, int S, int D, int causal, int dtype, int num_sms, 
     const int rc = check_args(B, H, S, D, causal, dtype);
     if (rc != FA_OK) return rc;
     plan(B, H, S, D, causal, num_sms, info, nullptr);
+    return FA_OK;
+}
+
+int fa_fwd_schedule_table(int B, int H, int S, int D, int causal, int dtype, int num_sms, unsigned short* offsets,
+                          int offsets_cap, unsigned short* units, int units_cap, int* n_ctas, int* n_units)
+{
+    if (!offsets || !units || !n_ctas || !n_units || num_sms < 1 || offsets_cap < 0 || units_cap < 0)
+        return FA_ERR_INVALID_ARG;
+    const int rc = check_args(B, H, S, D, causal, dtype);
+    if (rc != FA_OK) return rc;
+    std::vector<fa::Params> hold(1);   // the table makes Params large: keep it off the stack
+    fa::Params* p = hold.data();
+    fa_launch_info_t info;
+    plan(B, H, S, D, causal, num_sms, &info, p);
+    if (p->sched != fa::kSchedTable) return FA_ERR_UNSUPPORTED;
+    const int nu = (int)p->tab_off[info.grid];
+    if (offsets_cap < info.grid + 1 || units_cap < nu) return FA_ERR_INVALID_ARG;
+    std::copy(p->tab_off, p->tab_off + info.grid + 1, offsets);
+    std::copy(p->tab_unit, p->tab_unit + nu, units);
+    *n_ctas = info.grid;
+    *n_units = nu;
     return FA_OK;
 }
 

@@ -10,6 +10,11 @@ namespace fa {
 constexpr int kBM = 128;       // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;       // keys per K/V tile
 constexpr int kThreads = 512;  // 4 warpgroups: softmax x2, correction/epilogue, load+MMA
+// Table schedule capacity: the table travels in the kernel parameters (16-bit
+// unit indices and offsets), so it serves launches of up to this many units on
+// up to this many CTAs; larger launches use the closed-form schedules.
+constexpr int kSchedTableMaxUnits = 6144;
+constexpr int kSchedTableMaxCtas = 160;
 
 // Work-unit schedule and problem constants, identical for every CTA.
 struct Params {
@@ -24,7 +29,7 @@ struct Params {
     int tpu;                    // query tiles per work unit: 1 or 2
     int n_qgroups;              // ceil(n_qtiles / tpu)
     int n_units;                // BH * n_qgroups
-    int sched;                  // kSchedSnake or kSchedPairs
+    int sched;                  // kSchedSnake, kSchedPairs or kSchedTable
     int head_group;             // snake: heads whose units are interleaved, longest first
     int pairs_per_head;         // pairs: ceil(n_qgroups / 2)
     long long n_pairs;          // pairs: BH * pairs_per_head
@@ -44,6 +49,12 @@ struct Params {
     unsigned long long* trace;
     int trace_ctas;
     int trace_cap;
+    // Table schedule (kSchedTable): CTA c runs units tab_unit[tab_off[c]] ..
+    // tab_unit[tab_off[c + 1] - 1] in that order; a unit is bh * n_qgroups + qg.
+    // Kept last: the kernel takes Params as a __grid_constant__ parameter and
+    // reads the table from parameter space.
+    unsigned short tab_off[kSchedTableMaxCtas + 1];
+    unsigned short tab_unit[kSchedTableMaxUnits];
 };
 
 // Split-KV merge: one block per (batch*head, query tile) combines the tile's
@@ -84,7 +95,7 @@ enum TraceEvent : unsigned {
     kEvExit = 42,       // kernel: all roles done, before TMEM is freed
 };
 
-enum : int { kSchedSnake = 0, kSchedPairs = 1 };
+enum : int { kSchedSnake = 0, kSchedPairs = 1, kSchedTable = 2 };
 
 // Key tiles a query tile visits: all of them, or up to its diagonal when causal.
 __host__ __device__ inline int kv_tiles_of(int q_tile, int n_kv, int causal)

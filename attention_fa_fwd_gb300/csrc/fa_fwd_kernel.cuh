@@ -93,10 +93,10 @@ constexpr float kLn2 = 0.693147180559945309f;
 // (load + MMA).  The four add up to 512 = 65536 registers / 128 threads; the
 // splits are the spill-free ones ptxas -v reports for each head dim and type
 //
-template <int D, bool kBF16, bool kSplit, bool kDec> struct RegSplit {   // split-KV and decoupled kernels
+template <int D, bool kBF16, bool kSplit, bool kDec> struct RegSplit {   // D=128, and split-KV kernels
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80;
 };
-template <bool kBF16> struct RegSplit<64, kBF16, false, false> {
+template <bool kBF16, bool kDec> struct RegSplit<64, kBF16, false, kDec> {
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72;
 };
 template <int D, bool kBF16, bool kSplit, bool kDec>
@@ -213,6 +213,14 @@ __device__ __forceinline__ Unit unit_at(int r, const Params& p)
         }
         un.j0 = rem * p.split_chunk;
         un.id = ui;
+    } else if (p.sched == kSchedTable) {
+        // the host's list schedule: this CTA's units, in order
+        const int at = (int)p.tab_off[c] + r;
+        un.status = at >= (int)p.tab_off[c + 1] ? kUnitDone : kUnitOk;
+        const int u = un.status == kUnitOk ? (int)p.tab_unit[at] : 0;
+        bh = u / p.n_qgroups;
+        qg = u - bh * p.n_qgroups;
+        un.id = u;
     } else if (p.sched == kSchedPairs) {
         // 32-bit arithmetic: pair indices stay below 2^31 (a 64-bit division
         // would bring in a called subroutine and slowed the whole kernel)
@@ -849,7 +857,7 @@ template <int D, bool kBF16, bool kSplit, bool kDec>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const Params p)
+                  const __grid_constant__ Params p)
 {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];

@@ -170,7 +170,8 @@ typedef struct {
     int units;           /* work units = B*H * ceil(query tiles / tiles_per_unit) */
     int head_group;      /* snake schedule: heads scheduled together (longest units first) */
     int num_sms;         /* SM count of the current device */
-    int schedule;        /* 0 = snake over units, 1 = causal mirror pairs (see the kernel source) */
+    int schedule;        /* 0 = snake over units, 1 = causal mirror pairs, 2 = host list schedule
+                            (fa_fwd_schedule_table); see the kernel source */
 } fa_launch_info_t;
 
 /*
@@ -185,6 +186,26 @@ int fa_fwd_launch_info(int B, int H, int S, int D, int causal, int dtype, fa_lau
  * Pure host computation: touches no device, so it works without a GPU.
  */
 int fa_fwd_plan(int B, int H, int S, int D, int causal, int dtype, int num_sms, fa_launch_info_t* info);
+
+/*
+ * fa_fwd_schedule_table - the table schedule fa_fwd uses for a causal launch
+ * of several rounds (schedule == 2 in fa_fwd_plan) on a device with `num_sms`
+ * SMs.  Not on the pages: causal units differ in length ("CUDA手写masked
+ * multi-head attention", section 2.1: the upper triangle does no work), and the
+ * host balances them by longest-first list scheduling inside groups of heads
+ * whose K/V fit in L2 together; the table travels in the kernel parameters.
+ *
+ * Pure host computation (no device).  On success writes n_ctas + 1 offsets to
+ * offsets[] (capacity offsets_cap) and n_units unit indices to units[]
+ * (capacity units_cap): CTA c runs units[offsets[c]] .. units[offsets[c+1]-1]
+ * in that order, a unit index being bh * ceil(query tiles / tiles_per_unit) +
+ * query group.  Returns FA_OK; FA_ERR_UNSUPPORTED when the launch uses a
+ * closed-form schedule instead; FA_ERR_INVALID_ARG for a null pointer,
+ * num_sms < 1 or a buffer that is too small; otherwise as fa_fwd's checks.
+ */
+int fa_fwd_schedule_table(int B, int H, int S, int D, int causal, int dtype, int num_sms,
+                          unsigned short* offsets, int offsets_cap, unsigned short* units, int units_cap,
+                          int* n_ctas, int* n_units);
 
 /*
  * fa_device_status - status word of the bounded in-kernel waits.

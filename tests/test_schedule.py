@@ -1,6 +1,8 @@
 """Every schedule of the persistent kernel covers every output row exactly once
-and stays in parity: snake over head groups, mirror pairs (even and odd group
-counts), one unit per CTA, non-causal head order.  Outputs start as NaN, so a
+and stays in parity: the host's list-schedule table (two-tile and one-tile
+units), and beyond the table's capacity the closed forms: mirror pairs (odd
+group count: the middle group's second slot is skipped) and snake over head
+groups; one unit per CTA; non-causal head order.  Outputs start as NaN, so a
 row no unit wrote is caught."""
 import numpy as np
 import pytest
@@ -21,12 +23,15 @@ def _lib():
     fa.build()
 
 
-# B, H, S, D, dtype, causal, expected schedule on a 152-SM GB300 (0 snake, 1 pairs)
+# B, H, S, D, dtype, causal, expected schedule on a 152-SM GB300
+# (0 snake / head order, 1 mirror pairs, 2 table)
 CASES = [
-    (8, 32, 2048, 64, "fp16", True, 1),      # pairs, 8 query groups per head
-    (4, 96, 1664, 64, "bf16", True, 1),      # pairs, 7 groups: the middle group's second slot is skipped
-    (1, 40, 700, 128, "fp16", True, 1),      # pairs of one-tile units, ragged sequence
-    (2, 16, 4096, 128, "bf16", True, 0),     # snake, several rounds
+    (8, 32, 2048, 64, "fp16", True, 2),      # table, 8 query groups per head
+    (4, 96, 1664, 64, "bf16", True, 2),      # table, 7 groups (ragged last group of one tile)
+    (1, 40, 700, 128, "fp16", True, 2),      # table of one-tile units, ragged sequence
+    (2, 16, 4096, 128, "bf16", True, 2),     # table, long units
+    (8, 128, 1664, 64, "bf16", True, 1),     # beyond the table: pairs, 7 groups (middle slot skipped)
+    (8, 112, 1664, 64, "fp16", True, 0),     # beyond the table: snake over head groups
     (1, 16, 1024, 64, "fp16", True, 0),      # a single round: one unit per CTA
     (3, 24, 1000, 64, "bf16", False, 0),     # no mask: heads in order
 ]
