@@ -30,6 +30,8 @@ CASES = [
     (4, 96, 1664, 64, "bf16", True, 2),      # table, 7 groups (ragged last group of one tile)
     (1, 40, 700, 128, "fp16", True, 2),      # table of one-tile units, ragged sequence
     (2, 16, 4096, 128, "bf16", True, 2),     # table, long units
+    (16, 48, 2048, 64, "fp16", True, 2),     # table at its capacity: 6144 units
+    (3, 257, 2048, 64, "bf16", True, 1),     # 6168 units, just past the table: pairs
     (8, 128, 1664, 64, "bf16", True, 1),     # beyond the table: pairs, 7 groups (middle slot skipped)
     (8, 112, 1664, 64, "fp16", True, 0),     # beyond the table: snake over head groups
     (1, 16, 1024, 64, "fp16", True, 0),      # a single round: one unit per CTA
