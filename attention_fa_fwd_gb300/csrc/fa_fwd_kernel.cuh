@@ -186,6 +186,13 @@ enum : int { kUnitDone = 0, kUnitOk = 1, kUnitSkip = 2 };
 // head, so the CTAs of a round share few heads and the short unit re-reads K/V
 // the long one just brought into L2.  With an odd group count the middle group
 // pairs with itself and its second slot is skipped.
+//
+// kSchedTable (causal launches of several rounds, up to kSchedTableMaxUnits
+// units): the host's list schedule, carried in Params (per-CTA offsets and unit
+// indices bh * n_qgroups + qg); CTA c runs its list in order.  The host builds
+// it longest first inside groups of heads, each unit to the least loaded CTA.
+//
+// Split-KV launches take (head, query group, key chunk) units in dense order.
 // Returned by value: a unit the caller keeps by reference becomes
 // address-taken and its fields are reloaded from local memory in the MMA
 // issuer's inner loop (measured: 8% slower).
