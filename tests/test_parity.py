@@ -78,6 +78,13 @@ def test_long_sequence_sampled():
     check_sampled(1, 2, 32768 + 77, 128, "bf16", True)
 
 
+def test_very_long_sequence_sampled():
+    # 1025 query tiles, the last one ragged: 513 table units whose key loops
+    # run up to 1025 tiles; the fp32 row sums and O accumulate over 131k keys
+    assert _tiles_per_unit(1, 1, 131072 + 5, 64, True) == 2
+    check_sampled(1, 1, 131072 + 5, 64, "fp16", True)
+
+
 def test_causal_row0_is_v0_exactly():
     for D, dtype in ((64, "fp16"), (128, "bf16")):
         q, k, v = make_qkv(2, 3, 300, D, dtype, seed=3)
