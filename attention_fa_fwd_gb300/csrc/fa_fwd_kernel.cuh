@@ -753,6 +753,10 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         // K_j is entry kvb + 2(j - j0) of the ring, V_j the entry after it
         const uint32_t kvb = kv_count;
         FA_TRACE_EV(true, kTrMma, kEvUnit, un.id);
+        // the unit's first QKs, tile by tile: Q_1 frees only with the previous
+        // unit's very last QK and lands last, so QK_0 (and tile 0's softmax)
+        // need not wait for it
+        bool k_in = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (un.nkv[t] == 0) continue;
@@ -764,12 +768,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     goto done;
                 ph_sf ^= 1u << t;
             }
-        }
-        if (!kv_wait(kvb)) goto done;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (un.nkv[t] == 0) continue;
+            if (!k_in) {
+                if (!kv_wait(kvb)) goto done;
+                k_in = true;
+            }
+            ptx::tc_fence_after();
             issue_qk(t, kvb);
             ptx::mma_commit(bars + 8 * (kBarSFull + t));
             FA_TRACE_EV(true, kTrMma, kEvQK, (uint32_t)t << 12);
