@@ -10,6 +10,7 @@ returns an error status, the call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -100,6 +101,14 @@ def _stream_ptr(stream) -> int:
     return int(s.cuda_stream)
 
 
+def _on_device(device):
+    """Context that makes `device` current; a no-op when it already is (the
+    switch costs microseconds, comparable to a small problem's kernel)."""
+    if device.index is None or device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def _check_qkv(q, k, v):
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
@@ -137,7 +146,7 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
     if lse.shape != (B, H, S) or lse.dtype != torch.float32 or not lse.is_contiguous() \
             or lse.device != q.device:
         raise ValueError("lse must be a contiguous float32 [B, H, S] tensor on q's device")
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                           B, H, S, D, int(bool(causal)), float(scale), _DTYPE[q.dtype],
                           _stream_ptr(stream))
@@ -172,7 +181,7 @@ def fa_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bo
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         if workspace is None:
             need = splitkv_workspace_bytes(B, H, S, D, causal, q.dtype)
             workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -201,7 +210,7 @@ def fa_fwd_splitkv_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cau
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = lib().fa_fwd_splitkv_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                          lse.data_ptr(), B, H, S, D, int(bool(causal)), float(scale),
                                          _DTYPE[q.dtype], _stream_ptr(stream))
