@@ -98,3 +98,39 @@ def test_schedule_table_rejects_bad_arguments():
                                    ctypes.byref(n2)) == fa.FA_ERR_INVALID_ARG
     assert L.fa_fwd_schedule_table(4, 32, 4096, 96, 1, 1, 152, off, 4, units, 4, ctypes.byref(n1),
                                    ctypes.byref(n2)) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_table_cache_eviction_gives_the_same_table():
+    # more shapes than the host keeps tables for, then the first one again
+    first = fa.schedule_table(4, 32, 4096, 128, True, 152)
+    for h in range(20):
+        fa.schedule_table(2, 17 + h, 2048, 64, True, 152)
+    assert fa.schedule_table(4, 32, 4096, 128, True, 152) == first
+
+
+def test_concurrent_plans_agree_with_sequential_ones():
+    # the planner's caches are shared by every thread of the process (ctypes
+    # releases the GIL, so these calls run in the library at the same time)
+    import threading
+    shapes = [(4, 32, 4096, 128), (8, 16, 2048, 128), (1, 32, 16384, 128), (3, 40, 1500, 64), (2, 21, 3000, 64)]
+    want = {sh: fa.schedule_table(*sh, True, 152) for sh in shapes}
+    got, errors = {}, []
+
+    def worker(k):
+        try:
+            for i in range(30):
+                sh = shapes[(k + i) % len(shapes)]
+                t = fa.schedule_table(*sh, True, 152)
+                if t != want[sh]:
+                    errors.append(sh)
+                # new shapes too, so the caches insert and evict while others read
+                fa.plan(1 + (k + i) % 3, 9 + i, 1024 + 128 * k, 64, True, 152)
+        except Exception as e:  # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert errors == []
