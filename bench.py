@@ -48,12 +48,13 @@ def peaks():
 
 
 def source_hash() -> str:
-    """sha256 over the CUDA sources and the C header: identifies the kernel build."""
+    """sha256 over the kernel and launcher sources (csrc/): identifies the build
+    whose counters a profile summary holds.  The public header's comments do
+    not change the kernel, so they do not void a summary."""
     import glob
     import hashlib
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(ROOT, "attention_fa_fwd_gb300", "csrc", "*")))
-    files.append(os.path.join(ROOT, "include", "fa_fwd.h"))
     for fn in files:
         h.update(os.path.basename(fn).encode())
         with open(fn, "rb") as f:

@@ -13,8 +13,10 @@
  * The computation is tiled with online softmax ("FlashAttention的Triton性能考古学",
  * sections 核心算法回顾 and 关键优化：反转循环顺序: running max and sum per row,
  * one normalisation at the end), so the S x S score matrix never reaches device
- * memory, and uses the conditional rescale of "G6: Cluster 与 2CTA 探索", V41,
- * so O is rescaled only when a row's maximum rises by more than 2^8.
+ * memory, and uses the conditional rescale of "G6: Cluster 与 2CTA 探索", V41:
+ * a row keeps its base until its maximum rises by more than 2^15 (fp16) or 2^30
+ * (bf16) in scaled base-2 units (the page's 2^8, widened to what P's type holds),
+ * and O is rescaled only then, 32 rows at a time.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -26,10 +28,14 @@
  *            pinned host memory.  All tensor pointers must be 16-byte aligned.
  * Ownership  The caller allocates and frees every buffer.  The library
  *            allocates no device memory and keeps no per-call state; it caches
- *            one function-attribute setting and the SM count per device.
+ *            per device the SM count, the status word's address and each
+ *            kernel's shared-memory opt-in, and per shape the launch schedule
+ *            and the split-KV plan (host memory, guarded for concurrent use).
  * Streams    `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *            stream).  Work is enqueued on it and the call returns without
  *            synchronising; calls on different streams may run concurrently.
+ *            fa_fwd and fa_fwd_splitkv can be captured into CUDA graphs (the
+ *            kernels' parameters carry everything a launch needs).
  * Errors     Every entry point returns an fa_status_t and never aborts, throws
  *            or prints.  Invalid arguments are rejected before anything is
  *            enqueued.
@@ -54,7 +60,7 @@ typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,  /* null pointer, B/H/S < 1, causal not 0/1, scale not finite or <= 0,
                                 sizes overflowing 2^31 elements */
-    FA_ERR_UNSUPPORTED = 2,  /* D not in {64, 128}, unknown dtype, no sm_100-family device */
+    FA_ERR_UNSUPPORTED = 2,  /* D not in {64, 128}, unknown dtype, current device not compute capability 10.3 */
     FA_ERR_MISALIGNED = 3,   /* a tensor pointer not 16-byte aligned */
     FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, copy, tensor map) */
     FA_ERR_TIMEOUT = 5,      /* a bounded in-kernel wait gave up (reported by fa_device_status) */
