@@ -102,9 +102,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // heads per group), longest first inside a group, CTA c taking entries in snake
 // order (see unit_at / decode_unit in fa_fwd_kernel.cuh).  Larger groups balance
 // the causal triangle better; smaller groups keep the K/V of the heads in flight
-// within L2.  The planner replays the assignment for every group size whose K/V
-// fits the budget and keeps the best-balanced one (the smallest such group
-// within 0.5% of the best).  Results are cached per shape.
+// within L2.  The planner replays the assignment for the group sizes whose K/V
+// fits the budget (group_candidates) and keeps the best-balanced one (the
+// smallest such group within 0.5% of the best).  Results are cached per shape.
 
 constexpr long long kGroupKVBudget = 160ll << 20;   // bytes of K/V per group of heads
 
@@ -137,6 +137,20 @@ double snake_imbalance(int BH, int n_qtiles, int tpu, int n_qgroups, long long u
     return mx / (total / grid);
 }
 
+// Head-group sizes the planners replay: every size up to 32 (where the
+// balance moves most from one size to the next; the sizes picked for the
+// measured shapes are 4 to 26), then sizes about 12% apart up to `cap`.
+// Replaying every size up to the budget took seconds for launches of many
+// short heads (65536 heads of 128 keys: 5120 sizes x 65536 units).
+std::vector<int> group_candidates(long long cap)
+{
+    std::vector<int> c;
+    for (long long hg = 1; hg <= cap && hg <= 32; ++hg) c.push_back((int)hg);
+    for (long long hg = 36; hg < cap; hg = hg + hg / 8) c.push_back((int)hg);
+    if (cap > 32) c.push_back((int)cap);
+    return c;
+}
+
 int plan_head_group(int BH, int S, int D, int n_qtiles, int tpu, int n_qgroups, long long units, int grid)
 {
     struct Entry { int BH, S, D, grid, hg; };
@@ -151,16 +165,21 @@ int plan_head_group(int BH, int S, int D, int n_qtiles, int tpu, int n_qgroups, 
     long long cap = kGroupKVBudget / kv_head_bytes;
     if (cap < 1) cap = 1;
     if (cap > BH) cap = BH;
-    std::vector<double> load;
-    std::vector<double> score((size_t)cap + 1, 0.0);
-    double best = 1e30;
-    for (int hg = 1; hg <= cap; ++hg) {
-        score[(size_t)hg] = snake_imbalance(BH, n_qtiles, tpu, n_qgroups, units, grid, hg, load);
-        if (score[(size_t)hg] < best) best = score[(size_t)hg];
+    int pick = 1;   // one query group per head: every unit costs the same
+    if (n_qgroups > 1) {
+        const std::vector<int> cand = group_candidates(cap);
+        std::vector<double> load, score(cand.size());
+        double best = 1e30;
+        for (size_t i = 0; i < cand.size(); ++i) {
+            score[i] = snake_imbalance(BH, n_qtiles, tpu, n_qgroups, units, grid, cand[i], load);
+            best = std::min(best, score[i]);
+        }
+        for (size_t i = 0; i < cand.size(); ++i)
+            if (score[i] <= best + 0.005) {
+                pick = cand[i];
+                break;
+            }
     }
-    int pick = (int)cap;
-    for (int hg = 1; hg <= cap; ++hg)
-        if (score[(size_t)hg] <= best + 0.005) { pick = hg; break; }
     std::lock_guard<std::mutex> lock(mu);
     if (cache.size() >= 256) cache.erase(cache.begin());
     cache.push_back({BH, S, D, grid, pick});
@@ -174,8 +193,9 @@ int plan_head_group(int BH, int S, int D, int n_qtiles, int tpu, int n_qgroups, 
 // first inside a group, go one at a time to the CTA with the least modelled work
 // so far (a unit costs its key tiles plus two for its fixed part).  That is
 // longest-processing-time list scheduling per group.  Its balance moves with the
-// group size, so the planner replays it for every group whose K/V fits
-// kTableKVBudget and keeps the smallest group within 0.5% of the best.  It
+// group size, so the planner replays it for the group sizes whose K/V fits
+// kTableKVBudget (group_candidates) and keeps the smallest within 0.5% of the
+// best.  It
 // balances the causal triangle where mirror pairs leave rounds half-empty and a
 // snake needs all heads in one group (modelled, most loaded CTA over the mean:
 // 4x32x4096 1.04 pairs, 1.008 here with 8-head groups; 8x16x2048 1.19 pairs,
@@ -250,18 +270,22 @@ int table_plan(int BH, int S, int D, int n_qtiles, int tpu, int causal, int grid
         const long long kv_head_bytes = 2ll * S * D * 2;
         long long cap = kTableKVBudget / kv_head_bytes;
         cap = std::max(1ll, std::min(cap, (long long)BH));
-        std::vector<double> score((size_t)cap + 1, 0.0);
-        double best = 1e30;
-        for (int hg = 1; hg <= cap; ++hg) {
-            score[(size_t)hg] = list_schedule(BH, n_qtiles, tpu, causal, grid, hg, nullptr);
-            best = std::min(best, score[(size_t)hg]);
-        }
-        int pick = (int)cap;
-        for (int hg = 1; hg <= cap; ++hg)
-            if (score[(size_t)hg] <= best + 0.005) {
-                pick = hg;
-                break;
+        const int n_qgroups = (n_qtiles + tpu - 1) / tpu;
+        int pick = 1;   // one query group per head: every unit costs the same
+        if (n_qgroups > 1) {
+            const std::vector<int> cand = group_candidates(cap);
+            std::vector<double> score(cand.size());
+            double best = 1e30;
+            for (size_t i = 0; i < cand.size(); ++i) {
+                score[i] = list_schedule(BH, n_qtiles, tpu, causal, grid, cand[i], nullptr);
+                best = std::min(best, score[i]);
             }
+            for (size_t i = 0; i < cand.size(); ++i)
+                if (score[i] <= best + 0.005) {
+                    pick = cand[i];
+                    break;
+                }
+        }
         SchedTable n{BH, S, D, tpu, causal, grid, pick, {}, {}};
         std::vector<std::vector<unsigned short>> per;
         list_schedule(BH, n_qtiles, tpu, causal, grid, pick, &per);

@@ -134,3 +134,16 @@ def test_concurrent_plans_agree_with_sequential_ones():
     for t in threads:
         t.join()
     assert errors == []
+
+
+def test_planning_many_short_heads_is_fast():
+    # the planners replay a bounded set of group sizes: a first call for
+    # 65536 heads of 128 keys once took seconds (every size up to the budget)
+    import time
+    for shape in [(1, 65536, 128, 64), (48, 128, 128, 64), (8, 1024, 512, 64)]:
+        t0 = time.perf_counter()
+        fa.plan(*shape, True, 152)
+        assert time.perf_counter() - t0 < 1.0, shape
+    # the measured shapes keep their group sizes
+    assert fa.plan(4, 32, 4096, 128, True, 152)["head_group"] == 8
+    assert fa.plan(1, 32, 16384, 128, True, 152)["head_group"] == 4
