@@ -32,7 +32,7 @@ CASES = [
     (2, 16, 4096, 128, "bf16", True, 2),     # table, long units
     (16, 48, 2048, 64, "fp16", True, 2),     # table at its capacity: 6144 units
     (3, 257, 2048, 64, "bf16", True, 1),     # 6168 units, just past the table: pairs
-    (8, 128, 1664, 64, "bf16", True, 1),     # beyond the table: pairs, 7 groups (middle slot skipped)
+    (12, 112, 1152, 64, "bf16", True, 1),    # beyond the table: pairs, 5 groups (middle slot skipped)
     (8, 112, 1664, 64, "fp16", True, 0),     # beyond the table: snake over head groups
     (1, 16, 1024, 64, "fp16", True, 0),      # a single round: one unit per CTA
     (3, 24, 1000, 64, "bf16", False, 0),     # no mask: heads in order
