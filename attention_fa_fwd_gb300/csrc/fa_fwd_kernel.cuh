@@ -93,8 +93,11 @@ constexpr float kLn2 = 0.693147180559945309f;
 // (load + MMA).  The four add up to 512 = 65536 registers / 128 threads; the
 // splits are the spill-free ones ptxas -v reports for each head dim and type
 //
-template <int D, bool kBF16, bool kSplit, bool kDec> struct RegSplit {   // D=128, and split-KV kernels
+template <int D, bool kBF16, bool kSplit, bool kDec> struct RegSplit {   // D=128 one pass, D=64 split-KV
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80;
+};
+template <bool kBF16> struct RegSplit<128, kBF16, true, false> {
+    static constexpr uint32_t kSoftmax = 184, kEpilogue = 56, kControl = 88;
 };
 template <bool kBF16, bool kDec> struct RegSplit<64, kBF16, false, kDec> {
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72;
@@ -105,8 +108,9 @@ constexpr bool reg_split_fits()
     using R = RegSplit<D, kBF16, kSplit, kDec>;
     return 2 * R::kSoftmax + R::kEpilogue + R::kControl == 512;
 }
-static_assert(reg_split_fits<128, false, false, false>() && reg_split_fits<64, false, false, false>() &&
-                  reg_split_fits<64, false, false, true>(),
+static_assert(reg_split_fits<128, false, false, false>() && reg_split_fits<128, false, true, false>() &&
+                  reg_split_fits<64, false, false, false>() && reg_split_fits<64, false, false, true>() &&
+                  reg_split_fits<64, false, true, false>(),
               "register split must add up to 512");
 
 // Barrier indices inside the barrier array.
@@ -137,7 +141,13 @@ struct Cfg {
     static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
     static constexpr int kOffStage = kOffKV + kSlots * kTileBytes;   // one O box for the TMA store
     static constexpr int kOffStats = kOffStage + kBoxBytes;          // float4 (l, b, l_norm, 0) [2][128]
+    // Ring entries are freed in pairs: a step's V_j with the next K_{j+1}
+    // (they free together), a unit's last V with the next unit's first K, and
+    // entry 0 alone; pair p = (2p - 1, 2p) has barrier p % kPairs, one commit
+    // each.  (kSlots barriers are reserved; the first kPairs are used.)
+    static constexpr int kPairs = kSlots / 2;
     static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
+    __device__ static constexpr uint32_t pair_of(uint32_t entry) { return (entry + 1u) / 2u; }
     static constexpr int kNumBars = kBarKVEmpty + kSlots;
     static constexpr int kOffBars = kOffStats + 2 * kBM * 16;
     static constexpr int kOffCtl = kOffBars + kNumBars * 8;          // [0] TMEM base, [1] abort, [2] epilogue go
@@ -666,11 +676,14 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
             for (int kind = 0; kind < 2; ++kind) {
                 const uint32_t idx = kv_count;
                 const uint32_t slot = idx % C::kSlots;
-                const uint32_t use = idx / C::kSlots;
-                if (!ptx::mbar_wait(wc, bars + 8 * (C::kBarKVEmpty + slot), (use & 1u) ^ 1u,
-                                    kSiteLoad | (C::kBarKVEmpty + slot))) {
-                    ok = false;
-                    break;
+                if (idx >= (uint32_t)C::kSlots) {
+                    // the entry this copy overwrites must be freed: its pair's release
+                    const uint32_t pr = C::pair_of(idx - C::kSlots);
+                    const uint32_t b = C::kBarKVEmpty + pr % C::kPairs;
+                    if (!ptx::mbar_wait(wc, bars + 8 * b, (pr / C::kPairs) & 1u, kSiteLoad | b)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 ++kv_count;
                 const uint32_t fb = bars + 8 * (kBarKVFull + slot);
@@ -713,7 +726,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         return ptx::mbar_wait(wc, bars + 8 * (kBarKVFull + slot), (idx / C::kSlots) & 1u,
                               kSiteMma | (kBarKVFull + slot));
     };
-    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + idx % C::kSlots)); };
+    // frees the pair of ring entries ending at `idx` (see Cfg): one commit
+    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs)); };
     // S_t = Q_t K^T: M = 128 rows, N = 128 keys, K = D in steps of 16 (32 bytes
     // inside a 128-byte swizzled row; the next 64 columns sit in the next box).
     // Descriptors are built once per tile and stepped by adding the offset to
@@ -851,8 +865,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     }
                 }
             }
+            // V_j and K_{j+1} together; a unit's last V goes with the next
+            // unit's first K (released after that unit's first QKs)
             if (j + 1 < un.nmax) kv_release(ik);
-            kv_release(iv);
         }
         kv_count = kvb + 2 * (un.nmax - un.j0);
     }
