@@ -141,10 +141,17 @@ struct Cfg {
     static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
     static constexpr int kOffStage = kOffKV + kSlots * kTileBytes;   // one O box for the TMA store
     static constexpr int kOffStats = kOffStage + kBoxBytes;          // float4 (l, b, l_norm, 0) [2][128]
-    // Ring entries are freed in pairs: a step's V_j with the next K_{j+1}
-    // (they free together), a unit's last V with the next unit's first K, and
-    // entry 0 alone; pair p = (2p - 1, 2p) has barrier p % kPairs, one commit
-    // each.  (kSlots barriers are reserved; the first kPairs are used.)
+    // Ring entries free in pairs: V_j with the next K_{j+1} (they free
+    // together), a unit's last V with the next unit's first K, entry 0 alone;
+    // pair p = (2p - 1, 2p) has empty barrier p % kPairs, one commit each.
+    // At D=64 they also land in pairs (kFullPairs): a step's K_j and V_j,
+    // entries (2q, 2q+1), share full barrier q % kPairs (one arrival and one
+    // tile of bytes from each copy), so the wait for K_j before QK(j) also
+    // covers V_j for PV(j).  That makes QK(j+1) wait for V_{j+1} too: with the
+    // 8-slot ring there is slack for it, with D=128's 4 slots there is not
+    // (measured 5-9% slower there, 2-3% faster at D=64).  kSlots barriers are
+    // reserved per side.
+    static constexpr bool kFullPairs = (D == 64);
     static constexpr int kPairs = kSlots / 2;
     static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
     __device__ static constexpr uint32_t pair_of(uint32_t entry) { return (entry + 1u) / 2u; }
@@ -686,7 +693,7 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
                     }
                 }
                 ++kv_count;
-                const uint32_t fb = bars + 8 * (kBarKVFull + slot);
+                const uint32_t fb = bars + 8 * (kBarKVFull + (C::kFullPairs ? (idx / 2u) % C::kPairs : slot));
                 ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
                 const uint32_t dst = smem_base + C::kOffKV + slot * C::kTileBytes;
                 const CUtensorMap* m = kind ? tm_v : tm_k;
@@ -702,9 +709,21 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
     for (int t = 0; t < 2; ++t)
         if ((q_issued >> t) & 1u)
             ptx::mbar_wait_drain(wc, bars + 8 * (kBarQFull + t), ((ph_qe >> t) & 1u) ^ 1u, kSiteDrain | (kBarQFull + t));
-    for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < kv_count; ++s) {
-        const uint32_t last = kv_count - 1 - ((kv_count - 1 - s) % C::kSlots);   // last use of slot s
-        ptx::mbar_wait_drain(wc, bars + 8 * (kBarKVFull + s), (last / C::kSlots) & 1u, kSiteDrain | (kBarKVFull + s));
+    if (!C::kFullPairs) {
+        for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < kv_count; ++s) {
+            const uint32_t last = kv_count - 1 - ((kv_count - 1 - s) % C::kSlots);   // last use of slot s
+            ptx::mbar_wait_drain(wc, bars + 8 * (kBarKVFull + s), (last / C::kSlots) & 1u,
+                                 kSiteDrain | (kBarKVFull + s));
+        }
+    } else if (kv_count > 0) {
+        const uint32_t qmax = (kv_count - 1) / 2;   // the last pair with a copy issued
+        // a pair left with only its K copy (an abort in between) gets its
+        // second arrival here, so its phase completes once that copy lands
+        if (kv_count & 1u) ptx::mbar_arrive(bars + 8 * (kBarKVFull + qmax % C::kPairs));
+        for (uint32_t b = 0; b < (uint32_t)C::kPairs && b <= qmax; ++b) {
+            const uint32_t q = qmax - ((qmax - b) % C::kPairs);   // last pair on barrier b
+            ptx::mbar_wait_drain(wc, bars + 8 * (kBarKVFull + b), (q / C::kPairs) & 1u, kSiteDrain | (kBarKVFull + b));
+        }
     }
 }
 
@@ -721,10 +740,17 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     uint32_t kv_count = 0;
     FA_TRACE_DECL;
 
+    // at D=64 K_j and V_j land on one barrier (see Cfg): waiting for K_j (the
+    // unit's first QK, or QK(j) in the step before) also covers V_j for PV(j)
     auto kv_wait = [&](uint32_t idx) -> bool {
-        const uint32_t slot = idx % C::kSlots;
-        return ptx::mbar_wait(wc, bars + 8 * (kBarKVFull + slot), (idx / C::kSlots) & 1u,
-                              kSiteMma | (kBarKVFull + slot));
+        if constexpr (C::kFullPairs) {
+            const uint32_t q = idx / 2u, b = kBarKVFull + q % C::kPairs;
+            return ptx::mbar_wait(wc, bars + 8 * b, (q / C::kPairs) & 1u, kSiteMma | b);
+        } else {
+            const uint32_t slot = idx % C::kSlots;
+            return ptx::mbar_wait(wc, bars + 8 * (kBarKVFull + slot), (idx / C::kSlots) & 1u,
+                                  kSiteMma | (kBarKVFull + slot));
+        }
     };
     // frees the pair of ring entries ending at `idx` (see Cfg): one commit
     auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs)); };
@@ -795,7 +821,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         kv_release(kvb);
         for (int j = un.j0; j < un.nmax; ++j) {
             const uint32_t iv = kvb + 2 * (j - un.j0) + 1, ik = iv + 1;
-            bool v_ready = false, k_ready = false;
+            bool v_ready = C::kFullPairs, k_ready = false;
             if constexpr (kDec) {
                 // the next scores first: QK_t(j+1) needs only S_t(j) read into the
                 // softmax's registers, so it runs while that softmax computes P_t(j)
@@ -916,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(bars + 8 * kBarDrain, 1);
         for (int s = 0; s < C::kSlots; ++s) {
-            ptx::mbar_init(bars + 8 * (kBarKVFull + s), 1);
+            ptx::mbar_init(bars + 8 * (kBarKVFull + s), C::kFullPairs ? 2 : 1);   // (K_j's and V_j's copies)
             ptx::mbar_init(bars + 8 * (C::kBarKVEmpty + s), 1);
         }
         ctl[1] = 0u;
