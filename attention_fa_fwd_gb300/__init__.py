@@ -20,8 +20,8 @@ import torch
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "splitkv_workspace_bytes", "fa_fwd_hostio", "launch_info", "plan", "device_status",
-           "selftest_wait_timeout", "strerror", "build", "lib", "header_functions",
+__all__ = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "splitkv_workspace_bytes", "fa_fwd_hostio", "launch_info", "plan", "schedule_table", "device_status",
+           "selftest_wait_timeout", "selftest_exp2_poly", "strerror", "build", "lib", "header_functions",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_SCRATCH", "FaError"]
 
@@ -125,14 +125,9 @@ def _check_qkv(q, k, v):
         raise ValueError("q, k, v must be on one device")
 
 
-def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
-           scale: float | None = None, out: torch.Tensor | None = None,
-           lse: torch.Tensor | None = None, stream=None):
-    """O, LSE of softmax(Q K^T * scale + causal mask) V on the current CUDA stream.
-
-    q, k, v: contiguous CUDA [B, H, S, D] float16/bfloat16 (D in {64, 128}).
-    Returns (o [B, H, S, D] in the input dtype, lse [B, H, S] float32, natural log).
-    """
+def _prepare(q, k, v, scale, out, lse):
+    """Checks q, k, v and the output buffers (allocating those not given):
+    every buffer the kernels touch is exactly the size they assume."""
     _check_qkv(q, k, v)
     B, H, S, D = q.shape
     if scale is None:
@@ -141,11 +136,24 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
-    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != q.device:
+    if not isinstance(out, torch.Tensor) or out.shape != q.shape or out.dtype != q.dtype \
+            or not out.is_contiguous() or out.device != q.device:
         raise ValueError("out must be a contiguous tensor like q")
-    if lse.shape != (B, H, S) or lse.dtype != torch.float32 or not lse.is_contiguous() \
-            or lse.device != q.device:
+    if not isinstance(lse, torch.Tensor) or lse.shape != (B, H, S) or lse.dtype != torch.float32 \
+            or not lse.is_contiguous() or lse.device != q.device:
         raise ValueError("lse must be a contiguous float32 [B, H, S] tensor on q's device")
+    return B, H, S, D, scale, out, lse
+
+
+def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+           scale: float | None = None, out: torch.Tensor | None = None,
+           lse: torch.Tensor | None = None, stream=None):
+    """O, LSE of softmax(Q K^T * scale + causal mask) V on the current CUDA stream.
+
+    q, k, v: contiguous CUDA [B, H, S, D] float16/bfloat16 (D in {64, 128}).
+    Returns (o [B, H, S, D] in the input dtype, lse [B, H, S] float32, natural log).
+    """
+    B, H, S, D, scale, out, lse = _prepare(q, k, v, scale, out, lse)
     with _on_device(q.device):
         rc = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                           B, H, S, D, int(bool(causal)), float(scale), _DTYPE[q.dtype],
@@ -173,18 +181,14 @@ def fa_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bo
     split into chunks whose partial results are merged by a second kernel.
     `workspace` (a CUDA byte tensor) defaults to a fresh torch allocation of
     the size splitkv_workspace_bytes reports."""
-    _check_qkv(q, k, v)
-    B, H, S, D = q.shape
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    B, H, S, D, scale, out, lse = _prepare(q, k, v, scale, out, lse)
     with _on_device(q.device):
         if workspace is None:
             need = splitkv_workspace_bytes(B, H, S, D, causal, q.dtype)
             workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        if not isinstance(workspace, torch.Tensor) or workspace.device != q.device \
+                or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor on q's device")
         ws_bytes = workspace.numel() * workspace.element_size()
         rc = lib().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                   lse.data_ptr(), B, H, S, D, int(bool(causal)), float(scale),
@@ -202,14 +206,7 @@ def fa_fwd_splitkv_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cau
     device memory, the split scratch is a fixed 32 MiB array inside the library
     (shared by every call on a device; overlapping calls race on it).  Raises
     FaError with FA_ERR_SCRATCH when the problem needs more than that."""
-    _check_qkv(q, k, v)
-    B, H, S, D = q.shape
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    B, H, S, D, scale, out, lse = _prepare(q, k, v, scale, out, lse)
     with _on_device(q.device):
         rc = lib().fa_fwd_splitkv_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                          lse.data_ptr(), B, H, S, D, int(bool(causal)), float(scale),
@@ -224,16 +221,33 @@ def fa_fwd_hostio(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, causal: 
     """Host-buffer form: copies q/k/v in, runs the pass, copies o/lse out, all
     enqueued on the stream (the caller synchronises).  Host tensors should be
     pinned; device tensors are the caller's [B, H, S, D] / [B, H, S] buffers."""
+    host = {"q_h": q_h, "k_h": k_h, "v_h": v_h, "o_h": o_h, "lse_h": lse_h}
+    dev = {"q_d": q_d, "k_d": k_d, "v_d": v_d, "o_d": o_d, "lse_d": lse_d}
+    for name, t in list(host.items()) + list(dev.items()):
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor")
+    if q_h.dim() != 4:
+        raise ValueError("q_h must be [B, H, S, D]")
     B, H, S, D = q_h.shape
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
     dt = q_h.dtype
     if dt not in _DTYPE:
         raise ValueError("dtype must be float16 or bfloat16")
-    for t in (q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d):
-        if not t.is_contiguous():
-            raise ValueError("every buffer must be contiguous")
-    with torch.cuda.device(q_d.device):
+    for name in ("k_h", "v_h", "o_h", "q_d", "k_d", "v_d", "o_d"):
+        t = host.get(name, dev.get(name))
+        if t.shape != q_h.shape or t.dtype != dt:
+            raise ValueError(f"{name} must match q_h's shape and dtype")
+    for name, t in (("lse_h", lse_h), ("lse_d", lse_d)):
+        if t.shape != (B, H, S) or t.dtype != torch.float32:
+            raise ValueError(f"{name} must be a float32 [B, H, S] tensor")
+    for name, t in host.items():
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+    for name, t in dev.items():
+        if not t.is_cuda or t.device != q_d.device:
+            raise ValueError(f"{name} must be a CUDA tensor on q_d's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with _on_device(q_d.device):
         rc = lib().fa_fwd_hostio(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(),
                                  lse_h.data_ptr(), q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(),
                                  o_d.data_ptr(), lse_d.data_ptr(), B, H, S, D, int(bool(causal)),
@@ -296,7 +310,6 @@ def selftest_wait_timeout(timeout_us: int, stream=None) -> None:
 
 def selftest_exp2_poly(x, stream=None):
     """2^x by the FMA-pipe exponential, element-wise, for a CUDA float32 tensor."""
-    import torch
     if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32):
         raise TypeError("x must be a CUDA float32 tensor")
     x = x.contiguous()
