@@ -63,6 +63,25 @@ def test_head_dim_64_one_tile_per_unit(dtype, causal):
         check_full(B, H, S, 64, dtype, causal, seed=seed)
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D,scale", [(64, 2.0), (128, 2.0), (64, 1e-3), (128, 1e-3)])
+def test_extreme_scales(D, scale, causal, dtype):
+    """scale 2: scores of std 2*sqrt(D), rows close to one-hot, and the running
+    maximum jumps far past the re-base threshold at random key tiles; scale
+    1e-3: rows close to uniform, P's rounding spread over many keys."""
+    check_full(1, 2, 333, D, dtype, causal, seed=int(D + 1000 * scale), scale=scale)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D,dtype", [(64, "fp16"), (128, "bf16"), (128, "fp16"), (64, "bf16")])
+def test_stress_inputs_full(D, dtype, causal):
+    """The stress recipe (Q, K scaled by 3, key bias rising along the sequence,
+    so the row maximum keeps climbing and re-bases fire) at a size the oracle
+    checks in full: every row of every tile."""
+    check_full(1, 2, 700, D, dtype, causal, seed=3, kind="stress")
+
+
 def test_batch1_causal_workload_full():
     w = WORKLOADS["batch1_causal"]
     check_full(w.B, w.H, w.S, w.D, w.dtype, w.causal)
