@@ -58,6 +58,29 @@ def test_splitkv_parity_and_coverage(B, H, S, D, dtype, causal):
     assert (lse - l1).abs().max().item() <= TOL_LSE
 
 
+@pytest.mark.parametrize("B,H,S,D,dtype,causal,kind,scale", [
+    (1, 2, 2500, 64, "fp16", True, "stress", None),    # later chunks dominate every row
+    (1, 1, 4096, 128, "bf16", True, "stress", None),
+    (1, 4, 2048, 128, "bf16", True, "randn", 2.0),     # near one-hot rows: one chunk carries the row
+    (2, 1, 2000, 64, "fp16", False, "randn", 2.0),
+])
+def test_splitkv_merge_far_apart_partials(B, H, S, D, dtype, causal, kind, scale):
+    """The merge weights each chunk's partial O by exp(LSE_chunk - LSE_row):
+    with these inputs the partial LSEs of one row lie tens to hundreds apart,
+    so most weights underflow to 0 and one chunk carries the row."""
+    import oracle
+    from fa_inputs import to_f64
+    assert fa.splitkv_workspace_bytes(B, H, S, D, causal, _dt(dtype)) > 0
+    scale = scale if scale is not None else 1.0 / D ** 0.5
+    q, k, v = make_qkv(B, H, S, D, dtype, seed=7, kind=kind)
+    dq, dk, dv = (x.cuda() for x in (q, k, v))
+    o, lse = fa.fa_fwd_splitkv(dq, dk, dv, causal=causal, scale=scale)
+    assert fa.device_status() == (fa.FA_OK, 0)
+    o_ref, l_ref = oracle.attention(to_f64(q), to_f64(k), to_f64(v), causal, scale)
+    eo, el = errors(o.cpu(), lse.cpu(), o_ref, l_ref)
+    assert eo <= TOL_O[dtype] and el <= TOL_LSE, (eo, el)
+
+
 def test_workspace_reused_across_calls():
     # what a call leaves in the workspace must not leak into the next call
     B, H, S, D = 1, 8, 2048, 128
