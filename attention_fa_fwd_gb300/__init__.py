@@ -110,6 +110,16 @@ def _on_device(device):
 
 
 def _check_qkv(q, k, v):
+    # The valid case in one expression (a small problem's kernel takes less
+    # time than the call's host work); otherwise the failing check's message.
+    try:
+        shp, dt, dev = q.shape, q.dtype, q.device
+        if (q.is_cuda and len(shp) == 4 and k.shape == shp and v.shape == shp and k.dtype == dt
+                and v.dtype == dt and dt in _DTYPE and k.device == dev and v.device == dev
+                and q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+            return
+    except AttributeError:
+        pass
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
