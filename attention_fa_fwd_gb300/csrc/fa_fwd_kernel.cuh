@@ -922,9 +922,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     FA_TRACE_DECL;
     FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvEntry, 0);
-    // split-KV: the merge kernel may be scheduled now (it waits for this grid
-    // to complete before it reads anything)
-    if (kSplit && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // The next kernel in the stream (the split-KV merge, or the next pass) may
+    // be scheduled now: it waits for this grid to complete before it touches
+    // global memory, and meanwhile sets itself up on SMs this grid leaves.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -963,6 +964,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = ctl[0];
     const ptx::WaitCtx wc{base + C::kOffCtl + 4, p.timeout_ns, p.status};
+    // Launched as a programmatic dependent: the setup above (shared and tensor
+    // memory only) overlapped the previous grid's tail; every global access
+    // (inputs it may have written, outputs and workspace it may still read)
+    // comes after that grid has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvSetup, 0);
 
     if (warp < 8) {
@@ -1007,8 +1013,11 @@ int launch_instance(const LaunchArgs& a, cudaStream_t stream)
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
     return (int)e;
 }
