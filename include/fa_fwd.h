@@ -34,6 +34,10 @@
  * Streams    `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *            stream).  Work is enqueued on it and the call returns without
  *            synchronising; calls on different streams may run concurrently.
+ *            Each pass is launched as a programmatic dependent of the work
+ *            before it on the stream: its blocks may be scheduled while that
+ *            work finishes, but touch no global memory until it has
+ *            completed, so ordering on the stream is that of any kernel.
  *            fa_fwd and fa_fwd_splitkv can be captured into CUDA graphs (the
  *            kernels' parameters carry everything a launch needs).
  * Errors     Every entry point returns an fa_status_t and never aborts, throws
