@@ -127,6 +127,38 @@ def test_deterministic_and_stream_ordered():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("D,dtype", [(64, "fp16"), (128, "bf16")])
+def test_back_to_back_passes_order_through_memory(D, dtype):
+    """Passes launch as programmatic dependents of the work before them; the
+    stream order must still hold through memory.  Read after write: the
+    second pass takes the first pass's output as its queries.  Write after
+    read: a third pass writes its output over the first pass's queries,
+    which that pass may still be reading.  Each result must equal the same
+    calls with the GPU synchronised in between."""
+    B, H, S = 1, 16, 1024   # small passes: the next one launches while this one runs
+    q, k, v = (x.cuda() for x in make_qkv(B, H, S, D, dtype, seed=21))
+    q2, k2, v2 = (x.cuda() for x in make_qkv(B, H, S, D, dtype, seed=22))
+
+    def chain(sync):
+        qa = q.clone()
+        o1, l1 = fa.fa_fwd(qa, k, v, causal=True)
+        if sync:
+            torch.cuda.synchronize()
+        o2, l2 = fa.fa_fwd(o1, k, v, causal=True)        # reads pass 1's output
+        if sync:
+            torch.cuda.synchronize()
+        fa.fa_fwd(q2, k2, v2, causal=False, out=qa)       # overwrites pass 1's queries
+        torch.cuda.synchronize()
+        return o1.clone(), l1.clone(), o2.clone(), l2.clone(), qa.clone()
+
+    want = chain(True)
+    for _ in range(3):
+        got = chain(False)
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+    assert fa.device_status() == (fa.FA_OK, 0)
+
+
 def test_hostio_matches_device_path():
     q, k, v = make_qkv(2, 4, 333, 64, "fp16", seed=8)
     want_o, want_l = run_gpu(q, k, v, True, 0.125)
