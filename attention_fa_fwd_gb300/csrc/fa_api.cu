@@ -610,7 +610,7 @@ int check_call(const void* q, const void* k, const void* v, const void* o, const
 
 // One attention launch (and, with a split plan, the merge launch after it).
 int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D, int causal,
-            float scale, int dtype, int num_sms, const SplitPlan* sp, float* ws, void* stream)
+            float scale, int dtype, int num_sms, const SplitPlan* sp, float* ws, cudaStream_t s)
 {
     fa::LaunchArgs a;
     fa_launch_info_t info;
@@ -651,7 +651,6 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
         make_tmap(&a.tm_v, v, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_o, o, BH, S, D, dtype) != FA_OK)
         return FA_ERR_CUDA;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     int e;
     if (D == 64)
         e = dtype == FA_DTYPE_BF16 ? fa::launch_d64_bf16(a, s) : fa::launch_d64_f16(a, s);
@@ -683,7 +682,7 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
 extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D, int causal,
-           float scale, int dtype, void* stream)
+           float scale, int dtype, cudaStream_t stream)
 {
     int num_sms = 0;
     const int rc = check_call(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, &num_sms);
@@ -705,7 +704,7 @@ int fa_fwd_splitkv_workspace(int B, int H, int S, int D, int causal, int dtype, 
 }
 
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D,
-                   int causal, float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream)
+                   int causal, float scale, int dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream)
 {
     int num_sms = 0;
     const int rc = check_call(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, &num_sms);
@@ -769,7 +768,7 @@ int io_heads_per_chunk(int BH, size_t head_bytes)
 
 int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, void* q_d, void* k_d,
                   void* v_d, void* o_d, float* lse_d, int B, int H, int S, int D, int causal, float scale, int dtype,
-                  void* stream)
+                  cudaStream_t stream)
 {
     if (!q_h || !k_h || !v_h || !o_h || !lse_h || !q_d || !k_d || !v_d || !o_d || !lse_d)
         return FA_ERR_INVALID_ARG;
@@ -780,7 +779,7 @@ int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
     for (const void* p : ptrs)
         if (!aligned16(p)) return FA_ERR_MISALIGNED;
     const size_t n = (size_t)B * H * S * D * 2, nl = (size_t)B * H * S * sizeof(float);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t s = stream;
     const int BH = B * H;
     const size_t head_bytes = (size_t)S * D * 2, head_lse = (size_t)S * sizeof(float);
     const int hc = io_heads_per_chunk(BH, head_bytes);
@@ -835,9 +834,9 @@ int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
     return FA_OK;
 }
 
-int fa_device_status(void* stream, int clear, unsigned int* site)
+int fa_device_status(cudaStream_t stream, int clear, unsigned int* site)
 {
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
     unsigned int v = 0u;
     if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(v)) != cudaSuccess) return FA_ERR_CUDA;
     if (clear && v != 0u) {
@@ -848,22 +847,21 @@ int fa_device_status(void* stream, int clear, unsigned int* site)
     return v == 0u ? FA_OK : FA_ERR_TIMEOUT;
 }
 
-int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream)
+int fa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream)
 {
     if (timeout_us < 1u || timeout_us > 10000000u) return FA_ERR_INVALID_ARG;
     void* status = nullptr;
     if (cudaGetSymbolAddress(&status, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
-    const int e = fa::launch_wait_selftest(static_cast<unsigned int*>(status), (unsigned long long)timeout_us * 1000ull,
-                                           static_cast<cudaStream_t>(stream));
+    const int e = fa::launch_wait_selftest(static_cast<unsigned int*>(status), (unsigned long long)timeout_us * 1000ull, stream);
     return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_selftest_exp2_poly(const float* x, float* y, int n, void* stream)
+int fa_selftest_exp2_poly(const float* x, float* y, int n, cudaStream_t stream)
 {
     if (n < 0 || (n > 0 && (x == nullptr || y == nullptr))) return FA_ERR_INVALID_ARG;
     if (n == 0) return FA_OK;
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % alignof(float) != 0) return FA_ERR_MISALIGNED;
-    const int e = fa::launch_exp2_poly_selftest(x, y, n, static_cast<cudaStream_t>(stream));
+    const int e = fa::launch_exp2_poly_selftest(x, y, n, stream);
     return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -900,8 +898,7 @@ std::atomic<void*> g_static_scratch_ptr[kMaxDevices];
 int static_scratch(void** ptr)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
     void* p = g_static_scratch_ptr[dev].load(std::memory_order_acquire);
     if (!p) {
         if (cudaGetSymbolAddress(&p, g_fa_static_scratch) != cudaSuccess || !p) return FA_ERR_CUDA;
@@ -914,7 +911,7 @@ int static_scratch(void** ptr)
 }  // namespace
 
 extern "C" int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                                     int S, int D, int causal, float scale, int dtype, void* stream)
+                                     int S, int D, int causal, float scale, int dtype, cudaStream_t stream)
 {
     int num_sms = 0;
     int rc = check_call(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, &num_sms);

@@ -26,20 +26,27 @@
  * Pointers   "device" pointers must be addressable by the current CUDA device
  *            (cudaMalloc / torch CUDA tensors); "host" pointers are ordinary or
  *            pinned host memory.  All tensor pointers must be 16-byte aligned.
- * Ownership  The caller allocates and frees every buffer.  The library
- *            allocates no device memory and keeps no per-call state; it caches
- *            per device the SM count, the status word's address and each
- *            kernel's shared-memory opt-in, and per shape the launch schedule
- *            and the split-KV plan (host memory, guarded for concurrent use).
- * Streams    `stream` is a cudaStream_t passed as void* (NULL = legacy default
- *            stream).  Work is enqueued on it and the call returns without
- *            synchronising; calls on different streams may run concurrently.
- *            Each pass is launched as a programmatic dependent of the work
- *            before it on the stream: its blocks may be scheduled while that
- *            work finishes, but touch no global memory until it has
- *            completed, so ordering on the stream is that of any kernel.
- *            fa_fwd and fa_fwd_splitkv can be captured into CUDA graphs (the
- *            kernels' parameters carry everything a launch needs).
+ * Ownership  The caller allocates and frees every buffer; no call allocates
+ *            device memory.  Loading the library reserves, on every device
+ *            that runs any of its entry points, one static 32 MiB device
+ *            array: the scratch of fa_fwd_splitkv_static, which keeps the
+ *            partial results of the last split call made through that entry
+ *            point (see it for the sharing and race rules).  Beyond that the
+ *            library keeps no per-call state; it caches per device the SM
+ *            count, the status word's address and each kernel's shared-memory
+ *            opt-in, and per shape the launch schedule and the split-KV plan
+ *            (host memory, guarded for concurrent use).
+ * Streams    `stream` is a cudaStream_t (NULL = legacy default stream).  Work
+ *            is enqueued on it and the call returns without synchronising;
+ *            calls on different streams may run concurrently.  Each pass is
+ *            launched as a programmatic dependent of the work before it on
+ *            the stream: its blocks may be scheduled while that work
+ *            finishes, but touch no global memory until it has completed, so
+ *            ordering on the stream is that of any kernel.  fa_fwd,
+ *            fa_fwd_splitkv and fa_fwd_splitkv_static can be captured into
+ *            CUDA graphs (the kernels' parameters carry everything a launch
+ *            needs); fa_fwd_splitkv_static only after one uncaptured call on
+ *            the device, which looks up the address of its scratch array.
  * Errors     Every entry point returns an fa_status_t and never aborts, throws
  *            or prints.  Invalid arguments are rejected before anything is
  *            enqueued.
@@ -50,6 +57,12 @@
 #define FA_FWD_H
 
 #include <stddef.h>
+
+/* The CUDA runtime's stream handle, declared here so that this header needs no
+ * CUDA include; identical to the runtime's own typedef. */
+#ifndef __CUDA_RUNTIME_API_H__
+typedef struct CUstream_st* cudaStream_t;
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -81,12 +94,12 @@ typedef enum {
  *   causal   0 = no mask, 1 = key j allowed for query i iff j <= i
  *   scale    multiplier of Q K^T, finite and > 0 (usually 1/sqrt(D))
  *   dtype    an fa_dtype_t
- *   stream   cudaStream_t as void*
+ *   stream   the CUDA stream the work is enqueued on
  *
  * One kernel launch per call.  o and lse must not overlap q, k or v.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-           int B, int H, int S, int D, int causal, float scale, int dtype, void* stream);
+           int B, int H, int S, int D, int causal, float scale, int dtype, cudaStream_t stream);
 
 /*
  * fa_fwd_splitkv - fa_fwd for problems too small to fill the GPU in one pass.
@@ -113,7 +126,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  */
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int H, int S, int D, int causal, float scale, int dtype,
-                   void* workspace, size_t workspace_bytes, void* stream);
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * fa_fwd_splitkv_workspace - bytes of workspace fa_fwd_splitkv needs for this
@@ -146,7 +159,7 @@ int fa_fwd_splitkv_workspace(int B, int H, int S, int D, int causal, int dtype, 
  * already fits run as fa_fwd and use no scratch.
  */
 int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,
-                          int B, int H, int S, int D, int causal, float scale, int dtype, void* stream);
+                          int B, int H, int S, int D, int causal, float scale, int dtype, cudaStream_t stream);
 
 /*
  * fa_fwd_hostio - the same pass with host-side inputs and outputs.
@@ -169,7 +182,7 @@ int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, 
  */
 int fa_fwd_hostio(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
                   void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
-                  int B, int H, int S, int D, int causal, float scale, int dtype, void* stream);
+                  int B, int H, int S, int D, int causal, float scale, int dtype, cudaStream_t stream);
 
 /* Launch geometry fa_fwd would use for a problem on the current device. */
 typedef struct {
@@ -227,7 +240,7 @@ int fa_fwd_schedule_table(int B, int H, int S, int D, int causal, int dtype, int
  * returns FA_OK or FA_ERR_TIMEOUT; *site (if non-null) receives the recorded
  * site code (0 = none).  FA_ERR_CUDA if the synchronisation fails.
  */
-int fa_device_status(void* stream, int clear, unsigned int* site);
+int fa_device_status(cudaStream_t stream, int clear, unsigned int* site);
 
 /*
  * fa_selftest_wait_timeout - exercises the bounded wait used by the kernels.
@@ -238,7 +251,7 @@ int fa_device_status(void* stream, int clear, unsigned int* site);
  * once enqueued; read the outcome with fa_device_status.  Faults and hangs
  * nothing: the context stays usable.
  */
-int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream);
+int fa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream);
 
 /*
  * fa_selftest_exp2_poly - evaluates the FMA-pipe exponential the softmax can
@@ -257,7 +270,7 @@ int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream);
  * FA_ERR_MISALIGNED for a pointer not 4-byte aligned, FA_ERR_CUDA if the
  * launch fails.
  */
-int fa_selftest_exp2_poly(const float* x, float* y, int n, void* stream);
+int fa_selftest_exp2_poly(const float* x, float* y, int n, cudaStream_t stream);
 
 /* Human-readable text for an fa_status_t; never NULL. */
 const char* fa_strerror(int status);

@@ -80,3 +80,42 @@ def check_sampled(B, H, S, D, dtype, causal, seed=0, kind="randn"):
     assert eo <= TOL_O[dtype], f"max|dO| {eo:.3e} > {TOL_O[dtype]} on sampled rows"
     assert el <= TOL_LSE, f"max|dLSE| {el:.3e} > {TOL_LSE} on sampled rows"
     return eo, el
+
+
+def check_all_rows(B, H, S, D, dtype, causal, seed=0, kind="randn", heads_per_batch=4, nthreads=0):
+    """Full-size run on the GPU into NaN-filled outputs (a row no unit writes
+    stays NaN and fails), then every row of every head checked against the
+    oracle's row-by-row evaluation of the definition, a few heads at a time so
+    host memory stays bounded.  Returns (max|dO|, max|dLSE|)."""
+    q, k, v = make_qkv(B, H, S, D, dtype, seed, kind)
+    scale = 1.0 / D ** 0.5
+    dq, dk, dv = (x.cuda() for x in (q, k, v))
+    o = torch.full_like(dq, float("nan"))
+    lse = torch.full((B, H, S), float("nan"), device=dq.device, dtype=torch.float32)
+    fa.fa_fwd(dq, dk, dv, causal=causal, scale=scale, out=o, lse=lse)
+    status, site = fa.device_status(clear=True)
+    assert status == fa.FA_OK, f"in-kernel wait gave up at site {site:#x}"
+    del dq, dk, dv
+    BH = B * H
+    o_all = o.view(BH, S, D).cpu()
+    l_all = lse.view(BH, S).cpu()
+    del o, lse
+    assert torch.isfinite(o_all.float()).all(), "an output row was not written (NaN) or is not finite"
+    assert torch.isfinite(l_all).all(), "an LSE row was not written (NaN) or is not finite"
+    qf, kf, vf = (x.reshape(BH, S, D) for x in (q, k, v))
+    eo = el = 0.0
+    for h0 in range(0, BH, heads_per_batch):
+        h1 = min(BH, h0 + heads_per_batch)
+        sub = lambda x: to_f64(x[h0:h1].unsqueeze(0))
+        nh = h1 - h0
+        heads = np.repeat(np.arange(nh, dtype=np.int64), S)
+        rows = np.tile(np.arange(S, dtype=np.int64), nh)
+        o_ref, l_ref = oracle.attention_rows(sub(qf), sub(kf), sub(vf), causal, scale, heads, rows,
+                                             nthreads=nthreads)
+        o_got = o_all[h0:h1].reshape(nh * S, D).to(torch.float64).numpy()
+        l_got = l_all[h0:h1].reshape(nh * S).to(torch.float64).numpy()
+        eo = max(eo, float(np.max(np.abs(o_got - o_ref))))
+        el = max(el, float(np.max(np.abs(l_got - l_ref))))
+    assert eo <= TOL_O[dtype], f"max|dO| {eo:.3e} > {TOL_O[dtype]} over every row"
+    assert el <= TOL_LSE, f"max|dLSE| {el:.3e} > {TOL_LSE} over every row"
+    return eo, el

@@ -3,7 +3,8 @@ than one call's host work, so a caller captures the calls into a graph and
 replays it.  A captured fa_fwd or fa_fwd_splitkv (two kernels, the merge
 launched as a programmatic dependent) must replay with the inputs rewritten in
 place and give bit-for-bit the results of direct calls, and the graph must be
-replayable many times."""
+replayable many times.  fa_fwd_splitkv_static is captured after one
+uncaptured call, which looks up its scratch array's address."""
 import pytest
 import torch
 
@@ -72,4 +73,27 @@ def test_graph_replay_matches_direct_calls(B, H, S, D, dtype, causal, split):
         torch.cuda.synchronize()
         assert torch.equal(o, o_ref)
         assert torch.equal(lse, l_ref)
+    assert fa.device_status() == (fa.FA_OK, 0)
+
+
+def test_graph_replay_of_the_static_scratch_entry_point():
+    """fa_fwd_splitkv_static after one uncaptured call on the device (which
+    looks up the address of its scratch array): captured, replayed twice, it
+    gives bit for bit what the uncaptured call gave."""
+    B, H, S, D = 1, 1, 2500, 64
+    assert fa.splitkv_workspace_bytes(B, H, S, D, True, torch.float16) > 0
+    q, k, v = (x.cuda() for x in make_qkv(B, H, S, D, "fp16", seed=4))
+    o_ref, l_ref = fa.fa_fwd_splitkv_static(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, S), float("nan"), device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        fa.fa_fwd_splitkv_static(q, k, v, causal=True, out=o, lse=lse)
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
     assert fa.device_status() == (fa.FA_OK, 0)

@@ -4,13 +4,16 @@ under another framework's allocator without access to it).  Its scratch is a
 fixed array inside the library, so these tests check that two calls in a row
 through the C ABI give what the workspace-taking entry point gives, and that a
 problem needing more scratch than the array holds is refused before anything
-is launched.  The file is named to run after every other test."""
+is launched.
+
+The file's name makes pytest collect it last, so a run that stops at its first
+failure (-x) has run every other test before this one; the tests pass alone in
+a fresh process as well, since the array is reserved when the library loads."""
 import pytest
 import torch
 
 import attention_fa_fwd_gb300 as fa
 from fa_inputs import make_qkv
-from parity_util import TOL_LSE, TOL_O
 
 pytestmark = pytest.mark.gpu
 
@@ -46,8 +49,10 @@ def test_two_calls_match_the_workspace_entry_point():
         torch.cuda.synchronize()
         assert fa.device_status() == (fa.FA_OK, 0)
         assert torch.isfinite(o_s.float()).all() and torch.isfinite(l_s).all()
-        assert (o_s.float() - o_w.float()).abs().max().item() <= TOL_O["fp16"]
-        assert (l_s - l_w).abs().max().item() <= TOL_LSE
+        # same plan, kernels and merge as the workspace call, and passes are
+        # deterministic: the results must agree bit for bit (a stale partial
+        # or an offset into the array would not)
+        assert torch.equal(o_s, o_w) and torch.equal(l_s, l_w)
 
 
 def test_too_large_for_the_static_scratch_is_refused():
