@@ -97,6 +97,62 @@ def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = N
     return lib
 
 
+def ptxas_report(jobs: int | None = None) -> list[dict]:
+    """Compiles every translation unit with ``-Xptxas -v`` (objects in a
+    scratch folder, the library untouched) and returns, per kernel instance,
+    ptxas's register count at launch, stack frame and spill bytes."""
+    import re
+    import shutil
+    import tempfile
+    tmp = tempfile.mkdtemp(prefix="fa_ptxas_")
+    try:
+        def one(src):
+            obj = os.path.join(tmp, os.path.basename(src) + ".o")
+            cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj, "-Xptxas", "-v"]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
+            return os.path.basename(src), r.stderr
+        srcs = sources()
+        with ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
+            logs = list(ex.map(one, srcs))
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+    rows = []
+    for unit, log in logs:
+        cur = None
+        for line in log.splitlines():
+            m = re.search(r"Compiling entry function '(\S+)'", line)
+            if m:
+                cur = {"unit": unit, "mangled": m.group(1)}
+                continue
+            m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads", line)
+            if m and cur is not None:
+                cur["stack"], cur["spill_stores"], cur["spill_loads"] = (int(x) for x in m.groups())
+                continue
+            m = re.search(r"Used (\d+) registers", line)
+            if m and cur is not None:
+                cur["registers"] = int(m.group(1))
+                rows.append(cur)
+                cur = None
+    names = [r["mangled"] for r in rows]
+    try:
+        out = subprocess.run(["c++filt"], input="\n".join(names), capture_output=True, text=True,
+                             check=True).stdout.splitlines()
+    except (OSError, subprocess.CalledProcessError):
+        out = names
+    for r, n in zip(rows, out):
+        r["kernel"] = n.replace("(anonymous namespace)::", "").split("(")[0]
+    return rows
+
+
 if __name__ == "__main__":
     import sys
-    print(build(force=True, ptxas_verbose="-v" in sys.argv, trace="--trace" in sys.argv))
+    if "--ptxas-report" in sys.argv:
+        print("| translation unit | kernel | registers at launch | stack bytes | spill stores | spill loads |")
+        print("|---|---|---|---|---|---|")
+        for r in sorted(ptxas_report(), key=lambda r: (r["unit"], r["kernel"])):
+            print(f"| {r['unit']} | `{r['kernel']}` | {r['registers']} | {r['stack']} | {r['spill_stores']} | "
+                  f"{r['spill_loads']} |")
+    else:
+        print(build(force=True, ptxas_verbose="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -63,25 +63,20 @@ def source_hash() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this workload, or
-    None when there is none or it was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.md")
+    """DRAM bytes per launch from the committed ncu figures of this workload
+    (profiles/fa_fwd_kernel_<workload>.traffic.json), or None when there are
+    none or they were taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.traffic.json")
     try:
         with open(path, encoding="utf-8") as f:
-            text = f.read()
-    except OSError:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    fields = {}
-    for line in text.splitlines():
-        line = line.strip().strip("`")
-        if ":" in line:
-            k, v = line.split(":", 1)
-            fields[k.strip()] = v.strip()
-    if fields.get("source_sha256") != source_hash():
+    if rec.get("source_sha256") != source_hash():
         return None
     try:
-        return int(fields["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return int(rec["traffic_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -262,6 +257,92 @@ def run_reference(args, w):
     return 0
 
 
+# Every workload of the target list, timed on the device in the same run.  The
+# short ones are launch-bound, so each is timed for a fixed wall time instead of
+# a fixed count; C1 runs both masks.
+PER_CONFIG = [("C1", "tiny"), ("C1", "tiny_causal"), ("C2", "batch1_causal"), ("C3", "wide_noncausal"),
+              ("C4", "train_causal"), ("C5", "stress_causal")]
+
+
+def time_device_loop(step, stream, dev, steps):
+    """Milliseconds per step over `steps` back-to-back steps (CUDA events on the
+    launching stream, the device synchronised on both sides)."""
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps
+
+
+def per_config_lines(fa, dev, local, stream, peak_burst, peak_sustained, target_s):
+    """Device time, TFLOPS and fraction of peak of every workload, each timed
+    for about `target_s` seconds after a warm-up, with its own clock samples."""
+    out = {}
+    for tag, name in PER_CONFIG:
+        w = WORKLOADS[name]
+        q, k, v = make_workload(w)
+        qd, kd, vd = (x.to(dev) for x in (q, k, v))
+        od = torch.empty_like(qd)
+        ld = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+
+        def step():
+            fa.fa_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld, stream=stream)
+
+        for _ in range(5):
+            step()
+        probe = time_device_loop(step, stream, dev, 10)
+        steps = int(min(200000, max(20, target_s * 1e3 / max(probe, 1e-3))))
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.25)
+        ms = time_device_loop(step, stream, dev, steps)
+        clocks = sampler.stop()
+        status, site = fa.device_status(clear=True, stream=stream)
+        if status != fa.FA_OK:
+            raise SystemExit(f"{name}: in-kernel wait gave up at site {site:#x}")
+        tflops = w.flops() / (ms * 1e-3) / 1e12
+        out[name] = {"config": tag, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
+                     "dtype": w.dtype, "kind": w.kind, "steps": steps, "ms_per_step": round(ms, 6),
+                     "tflops": round(tflops, 3), "frac_burst": round(tflops / peak_burst, 4),
+                     "frac_sustained": round(tflops / peak_sustained, 4),
+                     "timed_s": round(ms * steps / 1e3, 3), "clocks": clocks}
+        del qd, kd, vd, od, ld
+        torch.cuda.empty_cache()
+    return out
+
+
+def e2e_leg(fa, w, q, k, v, qd, kd, vd, od, ld, stream, barrier, world, dist, dev, steps):
+    """The metric through fa_fwd_hostio with pinned host buffers: every step
+    copies q, k, v in and o, lse out around the pass."""
+    qh, kh, vh = (x.pin_memory() for x in (q, k, v))
+    oh = torch.empty_like(qh).pin_memory()
+    lh = torch.empty((w.B, w.H, w.S), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(steps, 50))
+
+    def e2e_step():
+        fa.fa_fwd_hostio(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, causal=w.causal, scale=w.scale,
+                         stream=stream)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    _, value = aggregate(e0.elapsed_time(e1) / e2e_steps, w.flops(), world, dist, dev)
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    return {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
 def run_ours(args, w):
     import attention_fa_fwd_gb300 as fa
     rank, world, local = dist_env()
@@ -326,28 +407,9 @@ def run_ours(args, w):
 
     # end to end through the C ABI with host buffers: H2D of q, k, v, the
     # kernel, D2H of o and lse, every step
-    qh, kh, vh = (x.pin_memory() for x in (q, k, v))
-    oh = torch.empty_like(qh).pin_memory()
-    lh = torch.empty((w.B, w.H, w.S), dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 50))
-
-    def e2e_step():
-        fa.fa_fwd_hostio(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, causal=w.causal, scale=w.scale,
-                         stream=stream)
-
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    barrier()
-    _, e2e_value = aggregate(e0.elapsed_time(e1) / e2e_steps, flops, world, dist, dev)
-    h2d = 3 * q.numel() * q.element_size()
-    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_leg(fa, w, q, k, v, qd, kd, vd, od, ld, stream, barrier, world, dist, dev, args.steps)
 
     if rank != 0:
         if dist is not None:
@@ -355,14 +417,14 @@ def run_ours(args, w):
         return 0
 
     pk, pk_kind = peaks()
+    burst = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     # a loop timed for half a second or more runs at the power-capped clock:
     # compare it with the sustained GEMM peak, a short burst with the burst peak
     if ms_max >= 500.0:
-        peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-        peak_kind = f"bf16 dense sustained ({pk_kind})"
+        peak, peak_kind = sustained, f"bf16 dense sustained ({pk_kind})"
     else:
-        peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        peak_kind = f"bf16 dense burst ({pk_kind})"
+        peak, peak_kind = burst, f"bf16 dense burst ({pk_kind})"
     traffic = args.traffic if args.traffic is not None else profiled_traffic(w.name)
     achieved = flops / (ms_step * 1e-3) / 1e12   # one launch per step on this stream
     line = {
@@ -380,8 +442,7 @@ def run_ours(args, w):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind, "timed_ms": round(ms_max, 1), "traffic": traffic},
-        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": args.steps * world,
         "clocks": clocks,
     }
@@ -394,6 +455,13 @@ def run_ours(args, w):
         line["cpu_baseline"] = None
     if w.kind == "stress" and not args.no_cpu_baseline:
         line["rescale"] = rescale_events(w, q, k, v)
+    if not args.no_per_config and world == 1:
+        del qd, kd, vd, od, ld
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config_lines(fa, dev, local, stream, burst, sustained, args.per_config_s)
+        line["per_config_peaks"] = {"burst": burst, "sustained": sustained, "kind": pk_kind,
+                                    "note": "fp16 workloads are compared with the bf16 dense peak "
+                                            "(the same tensor rate; only bf16 was measured)"}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -410,6 +478,11 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer leg (its chunked launches would mix into an ncu launch list)")
+    ap.add_argument("--no-per-config", action="store_true", help="time only the selected workload")
+    ap.add_argument("--per-config-s", type=float, default=0.5,
+                    help="seconds each workload of the per-config table is timed for")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
