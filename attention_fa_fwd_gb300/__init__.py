@@ -22,6 +22,7 @@ from . import _build
 
 __all__ = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "splitkv_workspace_bytes", "fa_fwd_hostio", "launch_info", "plan", "schedule_table", "device_status",
            "selftest_wait_timeout", "selftest_exp2_poly", "strerror", "build", "lib", "header_functions",
+           "set_layout", "layout", "LAYOUT_AUTO", "LAYOUT_TWO_TILE", "LAYOUT_ONE_TILE",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_SCRATCH", "FaError"]
 
@@ -42,7 +43,8 @@ class FaError(RuntimeError):
 class LaunchInfo(ctypes.Structure):
     _fields_ = [("grid", ctypes.c_int), ("block", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("tiles_per_unit", ctypes.c_int), ("units", ctypes.c_int),
-                ("head_group", ctypes.c_int), ("num_sms", ctypes.c_int), ("schedule", ctypes.c_int)]
+                ("head_group", ctypes.c_int), ("num_sms", ctypes.c_int), ("schedule", ctypes.c_int),
+                ("layout", ctypes.c_int), ("key_step", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -75,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.fa_device_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint)]
         L.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
         L.fa_selftest_exp2_poly.argtypes = [vp, vp, i, vp]
+        L.fa_fwd_set_layout.argtypes = [i]
+        L.fa_fwd_set_layout.restype = i
         L.fa_strerror.argtypes = [i]
         L.fa_strerror.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_fwd_hostio", "fa_fwd_launch_info", "fa_fwd_plan", "fa_fwd_schedule_table",
@@ -90,6 +94,28 @@ def header_functions() -> list[str]:
     with open(HEADER, encoding="utf-8") as fh:
         text = fh.read()
     return sorted(set(re.findall(r"^(?:int|const char\*|size_t)\s+(fa_\w+)\s*\(", text, re.M)))
+
+
+LAYOUT_AUTO, LAYOUT_TWO_TILE, LAYOUT_ONE_TILE = 0, 1, 2
+
+
+def set_layout(layout: int) -> int:
+    """Process-wide kernel layout of one-pass launches (0 automatic, 1 two query
+    tiles per unit, 2 one query tile per unit); returns the previous one."""
+    prev = lib().fa_fwd_set_layout(int(layout))
+    if prev < 0:
+        raise ValueError(f"layout must be 0, 1 or 2, got {layout}")
+    return prev
+
+
+@contextlib.contextmanager
+def layout(value: int):
+    """Context in which one-pass launches use kernel layout `value`."""
+    prev = set_layout(value)
+    try:
+        yield
+    finally:
+        set_layout(prev)
 
 
 def strerror(status: int) -> str:

@@ -31,6 +31,17 @@ int g_trace_ctas = 0, g_trace_cap = 0;
 #endif
 
 constexpr int kMaxDevices = 64;
+
+// Kernel layout of one-pass launches (fa_fwd_set_layout): 0 = automatic.
+std::atomic<int> g_layout{0};
+constexpr int kLayoutAuto = 0, kLayoutTwoTile = 1, kLayoutOneTile = 2;
+
+// The layout a one-pass launch of head dim D uses.
+int resolve_layout(int /*D*/)
+{
+    const int l = g_layout.load(std::memory_order_relaxed);
+    return l == kLayoutAuto ? kLayoutTwoTile : l;
+}
 std::atomic<int> g_num_sms[kMaxDevices];     // 0 = not queried yet
 std::atomic<int> g_cc[kMaxDevices];          // major*10 + minor, 0 = not queried yet
 std::atomic<void*> g_status_addr[kMaxDevices];   // device address of g_fa_status, nullptr = not looked up
@@ -306,14 +317,17 @@ int table_plan(int BH, int S, int D, int n_qtiles, int tpu, int causal, int grid
     return t->hg;
 }
 
-// Work-unit geometry (see the schedule comment in fa_fwd_kernel.cuh).
-void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t* info, fa::Params* p)
+// Work-unit geometry (see the schedule comment in fa_fwd_kernel.cuh).  The
+// one-tile layout (fa_fwd_wide.cuh) always takes one query tile per unit.
+void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t* info, fa::Params* p,
+          int layout)
 {
     const int BH = B * H;
     const int n_qtiles = (S + kBM - 1) / kBM;
+    const bool one_tile = layout == kLayoutOneTile;
     // two query tiles per unit (ping-pong softmax) once there is enough work for
     // two units per SM; otherwise one, so small problems still fill the GPU
-    const int tpu = ((long long)BH * n_qtiles >= 2ll * num_sms) ? 2 : 1;
+    const int tpu = (!one_tile && (long long)BH * n_qtiles >= 2ll * num_sms) ? 2 : 1;
     const int n_qgroups = (n_qtiles + tpu - 1) / tpu;
     const long long units = (long long)BH * n_qgroups;
     const int grid = (int)(units < num_sms ? units : num_sms);
@@ -343,12 +357,14 @@ void plan(int B, int H, int S, int D, int causal, int num_sms, fa_launch_info_t*
     if (info) {
         info->grid = grid;
         info->block = fa::kThreads;
-        info->smem_bytes = fa::smem_bytes_for(D);
+        info->smem_bytes = one_tile ? fa::wide_smem_bytes_for(D) : fa::smem_bytes_for(D);
         info->tiles_per_unit = tpu;
         info->units = (int)units;
         info->head_group = head_group;
         info->num_sms = num_sms;
         info->schedule = table ? 2 : (pairs ? 1 : 0);
+        info->layout = one_tile ? kLayoutOneTile : kLayoutTwoTile;
+        info->key_step = one_tile ? fa::kWideBN : fa::kBN;
     }
     if (p) {
         p->BH = BH;
@@ -475,14 +491,14 @@ size_t split_workspace_bytes(const SplitPlan& sp, int D)
     return (size_t)sp.units * sp.tpu * kBM * (size_t)(D + 1) * sizeof(float);
 }
 
-// [B*H, S, D] 16-bit tensor, 128-row x 64-column boxes, 128-byte swizzle.
-int make_tmap(CUtensorMap* m, const void* ptr, int BH, int S, int D, int dtype)
+// [B*H, S, D] 16-bit tensor, `rows`-row x 64-column boxes, 128-byte swizzle.
+int make_tmap(CUtensorMap* m, const void* ptr, int BH, int S, int D, int dtype, int rows = kBM)
 {
     auto fn = encode_fn();
     if (!fn) return FA_ERR_CUDA;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(m, dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                           3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -553,7 +569,7 @@ int fa_fwd_launch_info(int B, int H, int S, int D, int causal, int dtype, fa_lau
     int num_sms = 0, cc = 0;
     rc = device_props(&num_sms, &cc);
     if (rc != FA_OK) return rc;
-    plan(B, H, S, D, causal, num_sms, info, nullptr);
+    plan(B, H, S, D, causal, num_sms, info, nullptr, resolve_layout(D));
     return FA_OK;
 }
 
@@ -562,8 +578,14 @@ int fa_fwd_plan(int B, int H, int S, int D, int causal, int dtype, int num_sms, 
     if (!info || num_sms < 1) return FA_ERR_INVALID_ARG;
     const int rc = check_args(B, H, S, D, causal, dtype);
     if (rc != FA_OK) return rc;
-    plan(B, H, S, D, causal, num_sms, info, nullptr);
+    plan(B, H, S, D, causal, num_sms, info, nullptr, resolve_layout(D));
     return FA_OK;
+}
+
+int fa_fwd_set_layout(int layout)
+{
+    if (layout < kLayoutAuto || layout > kLayoutOneTile) return -1;
+    return g_layout.exchange(layout);
 }
 
 int fa_fwd_schedule_table(int B, int H, int S, int D, int causal, int dtype, int num_sms, unsigned short* offsets,
@@ -576,7 +598,7 @@ int fa_fwd_schedule_table(int B, int H, int S, int D, int causal, int dtype, int
     std::vector<fa::Params> hold(1);   // the table makes Params large: keep it off the stack
     fa::Params* p = hold.data();
     fa_launch_info_t info;
-    plan(B, H, S, D, causal, num_sms, &info, p);
+    plan(B, H, S, D, causal, num_sms, &info, p, resolve_layout(D));
     if (p->sched != fa::kSchedTable) return FA_ERR_UNSUPPORTED;
     const int nu = (int)p->tab_off[info.grid];
     if (offsets_cap < info.grid + 1 || units_cap < nu) return FA_ERR_INVALID_ARG;
@@ -614,7 +636,8 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
 {
     fa::LaunchArgs a;
     fa_launch_info_t info;
-    plan(B, H, S, D, causal, num_sms, &info, &a.p);
+    const int layout = sp ? kLayoutTwoTile : resolve_layout(D);
+    plan(B, H, S, D, causal, num_sms, &info, &a.p, layout);
     a.grid = info.grid;
     if (cudaGetDevice(&a.device) != cudaSuccess || a.device < 0 || a.device >= kMaxDevices) return FA_ERR_CUDA;
     const int BH = B * H;
@@ -647,11 +670,23 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
         g_status_addr[a.device].store(status, std::memory_order_release);
     }
     a.p.status = static_cast<unsigned int*>(status);
+    int e;
+    if (layout == kLayoutOneTile) {
+        const int kv_rows = fa::kWideBN;
+        if (make_tmap(&a.tm_q, q, BH, S, D, dtype) != FA_OK ||
+            make_tmap(&a.tm_k, k, BH, S, D, dtype, kv_rows) != FA_OK ||
+            make_tmap(&a.tm_v, v, BH, S, D, dtype, kv_rows) != FA_OK)
+            return FA_ERR_CUDA;
+        if (D == 64)
+            e = dtype == FA_DTYPE_BF16 ? fa::launch_wide_d64_bf16(a, s) : fa::launch_wide_d64_f16(a, s);
+        else
+            e = dtype == FA_DTYPE_BF16 ? fa::launch_wide_d128_bf16(a, s) : fa::launch_wide_d128_f16(a, s);
+        return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
     if (make_tmap(&a.tm_q, q, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_k, k, BH, S, D, dtype) != FA_OK ||
         make_tmap(&a.tm_v, v, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_o, o, BH, S, D, dtype) != FA_OK)
         return FA_ERR_CUDA;
 
-    int e;
     if (D == 64)
         e = dtype == FA_DTYPE_BF16 ? fa::launch_d64_bf16(a, s) : fa::launch_d64_f16(a, s);
     else

@@ -134,6 +134,16 @@ int launch_d64_bf16_dec(const LaunchArgs& a, cudaStream_t s);
 int launch_d64_f16_split_dec(const LaunchArgs& a, cudaStream_t s);
 int launch_d64_bf16_split_dec(const LaunchArgs& a, cudaStream_t s);
 
+// One-tile layout (fa_fwd_wide.cuh): one 128-row query tile per unit, steps of
+// kWideBN keys.  LaunchArgs::tm_o is not used; its K and V maps have boxes of
+// kWideBN rows (the kernel's expected bytes per copy assume exactly that).
+constexpr int kWideBN = 192;
+int launch_wide_d64_f16(const LaunchArgs& a, cudaStream_t s);
+int launch_wide_d64_bf16(const LaunchArgs& a, cudaStream_t s);
+int launch_wide_d128_f16(const LaunchArgs& a, cudaStream_t s);
+int launch_wide_d128_bf16(const LaunchArgs& a, cudaStream_t s);
+int wide_smem_bytes_for(int D);
+
 // Dynamic shared memory of the instance for head dim D.
 int smem_bytes_for(int D);
 

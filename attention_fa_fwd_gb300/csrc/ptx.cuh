@@ -136,6 +136,49 @@ __device__ __forceinline__ bool mbar_wait_drain(const WaitCtx& w, uint32_t bar, 
     }
 }
 
+// Shared-memory word with release / acquire semantics at CTA scope: a step
+// counter one warp publishes after its data, another polls before reading it.
+__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Warp-uniform bounded wait until the counter at `addr` reaches `target`
+// (counters only grow); lane 0 polls, the outcome reaches every lane, and
+// __syncwarp orders lane 0's acquire before the other lanes' reads.  Same
+// give-up rules as mbar_wait.
+__device__ __forceinline__ bool flag_wait_warp(const WaitCtx& w, uint32_t addr, uint32_t target, uint32_t site)
+{
+    uint32_t ok = 1u;
+    if ((threadIdx.x & 31) == 0 && ld_acquire_shared(addr) < target) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (ld_acquire_shared(addr) >= target) break;
+            if ((it & 15u) == 0u) {
+                if (ld_shared_volatile(w.abort_addr) != 0u) {
+                    ok = 0u;
+                    break;
+                }
+                if (globaltimer_ns() - t0 > w.timeout_ns) {
+                    st_shared_volatile(w.abort_addr, 1u);
+                    atomicCAS(w.status, 0u, site);
+                    ok = 0u;
+                    break;
+                }
+            }
+        }
+    }
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0u;
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -195,6 +195,8 @@ typedef struct {
     int num_sms;         /* SM count of the current device */
     int schedule;        /* 0 = snake over units, 1 = causal mirror pairs, 2 = host list schedule
                             (fa_fwd_schedule_table); see the kernel source */
+    int layout;          /* 1 = two query tiles per unit, 2 = one query tile per unit (fa_fwd_set_layout) */
+    int key_step;        /* keys per step of a unit's key loop: 128 (layout 1) or 192 (layout 2) */
 } fa_launch_info_t;
 
 /*
@@ -209,6 +211,26 @@ int fa_fwd_launch_info(int B, int H, int S, int D, int causal, int dtype, fa_lau
  * Pure host computation: touches no device, so it works without a GPU.
  */
 int fa_fwd_plan(int B, int H, int S, int D, int causal, int dtype, int num_sms, fa_launch_info_t* info);
+
+/*
+ * fa_fwd_set_layout - the kernel layout of one-pass launches, process-wide.
+ *
+ * Not on the pages: two layouts of the same computation, kept side by side so
+ * they can be measured against each other.
+ *   0  automatic (the default): the library picks per launch
+ *   1  two 128-row query tiles per work unit, 128-key steps, the two softmax
+ *      warpgroups alternating between the tiles (the ping-pong of "G6: Cluster
+ *      与 2CTA 探索", V37-V39, on one CTA)
+ *   2  one query tile per work unit, 192-key steps, both softmax warpgroups on
+ *      the tile (each on half of a step's keys), scores and probabilities in
+ *      separate tensor-memory regions so the next step's Q K^T overlaps the
+ *      softmax
+ * Split-KV launches (fa_fwd_splitkv) always use layout 1.  Results agree to
+ * within rounding, not bit for bit, across layouts; each layout is
+ * deterministic.  Returns the previous setting, or -1 (nothing changed) for
+ * a value outside 0..2.  Calls already enqueued are not affected.
+ */
+int fa_fwd_set_layout(int layout);
 
 /*
  * fa_fwd_schedule_table - the table schedule fa_fwd uses for a causal launch
