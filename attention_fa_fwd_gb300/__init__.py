@@ -24,10 +24,10 @@ __all__ = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "splitkv_workspa
            "selftest_wait_timeout", "selftest_exp2_poly", "strerror", "build", "lib", "header_functions",
            "set_layout", "layout", "LAYOUT_AUTO", "LAYOUT_TWO_TILE", "LAYOUT_ONE_TILE",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
-           "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_SCRATCH", "FaError"]
+           "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_SCRATCH", "FA_ERR_RANGE", "FaError"]
 
 (FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_TIMEOUT,
- FA_ERR_SCRATCH) = range(7)
+ FA_ERR_SCRATCH, FA_ERR_RANGE) = range(8)
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
 HEADER = os.path.join(_build.ROOT, "include", "fa_fwd.h")
 
@@ -333,7 +333,7 @@ def device_status(clear: bool = True, stream=None) -> tuple[int, int]:
     """(status, site) of the bounded in-kernel waits; synchronises the stream."""
     site = ctypes.c_uint(0)
     rc = lib().fa_device_status(_stream_ptr(stream), int(bool(clear)), ctypes.byref(site))
-    if rc not in (FA_OK, FA_ERR_TIMEOUT):
+    if rc not in (FA_OK, FA_ERR_TIMEOUT, FA_ERR_RANGE):
         raise FaError(rc, "fa_device_status")
     return rc, site.value
 

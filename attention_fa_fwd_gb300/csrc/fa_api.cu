@@ -557,6 +557,7 @@ const char* fa_strerror(int status)
     case FA_ERR_CUDA: return "CUDA runtime/driver error";
     case FA_ERR_TIMEOUT: return "a bounded in-kernel wait timed out";
     case FA_ERR_SCRATCH: return "problem needs more split-KV scratch than the library's static array holds";
+    case FA_ERR_RANGE: return "bf16 input V holds a value beyond fp16's range (+-65504): results invalid";
     default: return "unknown status";
     }
 }
@@ -879,7 +880,8 @@ int fa_device_status(cudaStream_t stream, int clear, unsigned int* site)
         if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
     }
     if (site) *site = v;
-    return v == 0u ? FA_OK : FA_ERR_TIMEOUT;
+    if (v == 0u) return FA_OK;
+    return (v & 0xF00u) == fa::kSiteRangeV ? FA_ERR_RANGE : FA_ERR_TIMEOUT;
 }
 
 int fa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream)

@@ -13,10 +13,14 @@
 //   warps 0-3   softmax warpgroup of query tile 0 (one thread per row)
 //   warps 4-7   softmax warpgroup of query tile 1
 //   warps 8-11  correction/epilogue warpgroup: the final correction O / l,
-//               LSE, bf16/fp16 convert, shared-memory staging and TMA store
+//               LSE, bf16/fp16 convert, shared-memory staging and TMA store;
+//               for one-pass bf16 launches the softmax warpgroups run the
+//               epilogue (epi_in_softmax) and these warps convert V tiles
 //   warp 12     TMA producer: Q tiles, then a ring of K/V slots
 //   warp 13     tcgen05 MMA issuer (one thread) and TMEM owner
-//   warps 14-15 idle (they complete the fourth warpgroup for setmaxnreg)
+//   warps 14-15 bf16 inputs: convert V tiles to fp16 in shared memory (P is
+//               fp16, see p_is_bf16); fp16 inputs: idle (they complete the
+//               fourth warpgroup for setmaxnreg)
 //
 // A work unit is one (batch*head, group of 1 or 2 query tiles of 128 rows).  TMEM
 // (512 columns x 128 lanes, fp32) holds S0 | S1 | O0 | O1: the scores of each
@@ -65,6 +69,31 @@ namespace fa {
 template <bool kBF16>
 __host__ __device__ constexpr float rebase_threshold() { return kBF16 ? 30.0f : 15.0f; }
 
+// Where a re-base puts the base: the tile maximum plus this much (log2 units).
+// Any base gives the same result in real arithmetic; above the maximum, p
+// starts at 2^-overshoot <= 1 and the next re-base waits until the row maximum
+// rises by T + overshoot instead of T, which matters for fp16 P (T = 15) on
+// inputs whose maxima keep rising; p of 2^-20 of the row's largest stays
+// inside fp16's range (its subnormals reach 2^-24).
+template <bool kBF16>
+__host__ __device__ constexpr float rebase_overshoot() { return kBF16 ? 0.0f : 8.0f; }
+
+// P's 16-bit type.  P*V takes P and V of one type (tcgen05.mma kind::f16), and
+// bf16's 8-bit significand rounds P to 2^-9: on inputs whose rows are nearly
+// one-hot over large values of V that moves some elements of O past the
+// rounding midpoint of the bf16 output.  So for bf16 inputs two otherwise idle
+// warps convert each V tile to fp16 in shared memory once it lands
+// (vconvert_role), and P is fp16 for both input types; Q K^T stays bf16.
+// FA_BF16_P=1 builds keep bf16 P and V (the build option exists to measure
+// the conversion's cost).
+#ifndef FA_BF16_P
+#define FA_BF16_P 0
+#endif
+template <bool kBF16>
+__host__ __device__ constexpr bool p_is_bf16() { return kBF16 && FA_BF16_P != 0; }
+template <bool kBF16>
+__host__ __device__ constexpr bool converts_v() { return kBF16 && FA_BF16_P == 0; }
+
 // Pairs out of every 16 whose exponentials use ptx::f2_exp2_poly (the FMA
 // pipe) instead of ex2.approx (the XU): the split of the exponential work the
 // "Triton" page's MIO-bottleneck section motivates.  Off by default: on GB300
@@ -86,6 +115,17 @@ constexpr int kExp2PolyPairs = FA_EXP2_POLY_PAIRS;
 #define FA_EPILOGUE_IN_SOFTMAX 0
 #endif
 constexpr bool kEpilogueInSoftmax = FA_EPILOGUE_IN_SOFTMAX != 0;
+
+// Where the epilogue runs: in the softmax warpgroups with the V44 build option
+// (split-KV instances keep the separate epilogue: it writes the fp32
+// partials).  The conversion of V tiles (bf16 inputs) takes warps 14-15; the
+// epilogue warpgroup in the softmax warpgroups and all six warps converting
+// measured slower (train 1105 vs 1125, stress 1140 vs 1235 TFLOPS): the
+// conversion's cost is issue slots, not latency.
+template <bool kBF16, bool kSplit>
+__host__ __device__ constexpr bool epi_in_softmax() { return kEpilogueInSoftmax && !kSplit; }
+template <bool kBF16, bool kSplit>
+__host__ __device__ constexpr int conv_warps() { return converts_v<kBF16>() ? (epi_in_softmax<kBF16, kSplit>() ? 6 : 2) : 0; }
 static_assert(kExp2PolyPairs >= 0 && kExp2PolyPairs <= 16, "FA_EXP2_POLY_PAIRS must be in [0, 16]");
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -155,7 +195,11 @@ struct Cfg {
     static constexpr int kPairs = kSlots / 2;
     static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
     __device__ static constexpr uint32_t pair_of(uint32_t entry) { return (entry + 1u) / 2u; }
-    static constexpr int kNumBars = kBarKVEmpty + kSlots;
+    // [slots] a V tile converted to fp16 in place (bf16 inputs; 2 warps).  K
+    // and V alternate through an even number of slots, so V tiles always use
+    // the odd slots and each of these barriers completes once per V tile there.
+    static constexpr int kBarVConv = kBarKVEmpty + kSlots;
+    static constexpr int kNumBars = kBarVConv + kSlots;
     static constexpr int kOffBars = kOffStats + 2 * kBM * 16;
     static constexpr int kOffCtl = kOffBars + kNumBars * 8;          // [0] TMEM base, [1] abort, [2] epilogue go
     static constexpr int kSmemBytes = kOffCtl + 16 + 1024;            // + slack to align the base to 1 KB
@@ -314,6 +358,9 @@ __device__ __forceinline__ void trace_event(const Params& p, int role, uint32_t&
 #endif
 
 // Wait-site codes recorded in the status word: role << 8 | barrier index.
+// Status word of a CTA that found O not finite with bf16 inputs: V held a value
+// beyond fp16's range (its P*V runs in fp16), or an input was not finite.
+constexpr uint32_t kSiteRangeV = 0x800;
 enum : uint32_t { kSiteSoftmax = 0x100, kSiteEpilogue = 0x300, kSiteLoad = 0x400, kSiteMma = 0x500,
                   kSiteDrain = 0x600 };
 
@@ -353,12 +400,13 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
         if (nkv == 0) continue;
         float b = -INFINITY;   // base of the row, base-2 scaled units
         float l = 0.f;         // running sum of 2^(x - b): gives the LSE
-        // bf16: O is normalised by l + dl, where dl sums, per key tile, the
-        // rounding of the tile's largest p to bf16.  The MMAs weight V with the
-        // rounded P; when one key dominates a row, its rounding (up to 2^-9
-        // relative) would otherwise scale that row of O, and O rounded to bf16
-        // has no room left for it in the |dO| budget.  (fp16 rounds P to 2^-12
-        // and O to 2^-11 relative: dl stays 0 there.)
+        // bf16 inputs: O is normalised by l + dl, where dl sums, per key tile,
+        // the rounding of the tile's largest p to P's 16-bit type.  The MMAs
+        // weight V with the rounded P; when one key dominates a row, its
+        // rounding (2^-12 relative for fp16 P, 2^-9 for bf16 P) would otherwise
+        // scale that row of O, and a bf16 O in [4, 8) is already rounded to
+        // within 2^-6 (without dl the stress workload's worst row measured
+        // 1.1e-3 off).  fp16 inputs round O to 2^-11 relative: dl stays 0.
         float dl = 0.f;
         for (int j = un.j0; j < nkv; ++j) {
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + t), ph_s, kSiteSoftmax | (kBarSFull + t))) return;
@@ -411,12 +459,17 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             // own candidate at no extra cost: all 32 restart with the full
             // margin, and the next warp rescale waits for a row to climb T more.
             const float cand = fmaxf(b, mx);
-            const bool rebase = cand > b + rebase_threshold<kBF16>();
+            const bool rebase = cand > b + rebase_threshold<p_is_bf16<kBF16>()>();
             const bool rescale = j > un.j0 && __any_sync(0xffffffffu, rebase);
             float h = 1.f;
             if (rebase || rescale) {
-                h = ptx::ex2(b - cand);   // 0 on the first tile (b = -inf); 1 if cand == b
-                b = cand;
+                // a row that re-bases moves to its maximum plus the overshoot; a
+                // row the warp carries along only moves if that lies above its
+                // base (never by the overshoot again: repeated, that would push
+                // its p towards fp16's underflow)
+                const float nb_new = fmaxf(b, mx + rebase_overshoot<p_is_bf16<kBF16>()>());
+                h = ptx::ex2(b - nb_new);   // 0 on the first tile (b = -inf)
+                b = nb_new;
             }
             FA_TRACE_EV(tr, t, kEvMaxDone, j);
             if constexpr (kDec) {
@@ -449,7 +502,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             if constexpr (kBF16) {
                 // the tile maximum's p, by the same FMA and ex2 the loop below uses
                 const float pm = ptx::ex2(fmaf(mraw, sl2, nb));
-                dl = fmaf(dl, h, ptx::round16<kBF16>(pm) - pm);
+                dl = fmaf(dl, h, ptx::round16<p_is_bf16<kBF16>()>(pm) - pm);
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -466,7 +519,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                         p1 = ptx::ex2(x1);
                     }
                     acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
-                    pk[i] = ptx::pack2<kBF16>(p0, p1);
+                    pk[i] = ptx::pack2<p_is_bf16<kBF16>()>(p0, p1);
                 }
                 ptx::tmem_st16(tP + c * 16, pk);
                 if (c == 1 || c == 3) {
@@ -483,7 +536,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), sa, sb);
             l = fmaf(l, h, sa + sb);
         }
-        if constexpr (kEpilogueInSoftmax && !kSplit) {
+        if constexpr (epi_in_softmax<kBF16, kSplit>()) {
             // this tile's epilogue, here: O_t is final once its last PV completed
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarOFull + t), ph_o, kSiteSoftmax | (kBarOFull + t))) return;
             ph_o ^= 1u;
@@ -494,6 +547,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             const float inv_l = 1.0f / (l + dl);
             const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)un.bh * p.S + qrow) * D);
+            float osum = 0.f;   // converted V: a value beyond fp16's range makes O (and this sum) not finite
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
@@ -504,6 +558,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                     float x0, x1;
                     ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
                                    x0, x1);
+                    if constexpr (converts_v<kBF16>()) osum += fabsf(x0) + fabsf(x1);
                     pk[i] = ptx::pack2<kBF16>(x0, x1);
                 }
                 if (in) {
@@ -512,6 +567,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                         dst[c0 / 8 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
             }
+            if (converts_v<kBF16>() && in && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t));
@@ -545,7 +601,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
     volatile uint32_t* go = ctl_go;   // leader's wait outcome, read by all 128 threads
     uint32_t ph_o = 0u, ph_t = 0u;   // phase bit of tile t at bit t
     FA_TRACE_DECL;
-    if constexpr (kEpilogueInSoftmax && !kSplit) return;   // the softmax warpgroups run the epilogue
+    if constexpr (epi_in_softmax<kBF16, kSplit>()) return;   // the softmax warpgroups run the epilogue
 
     for (int r = 0;; ++r) {
         const Unit un = unit_at<kSplit>(r, p);
@@ -580,16 +636,20 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                 const size_t slot = ((size_t)un.id * p.tpu + t) * kBM + row;
                 float* dst = p.ws_o + slot * D;
                 const uint32_t tO = tmem + lane_base + C::col_o(t);
+                float osum = 0.f;   // converted V: a value beyond fp16's range makes O (and this sum) not finite
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
                     ptx::tmem_ld32_wait(tO + c0, o);
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(dst + c0 + i) =
-                            make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
-                                        __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 x = make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
+                                                     __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                        if constexpr (converts_v<kBF16>()) osum += (fabsf(x.x) + fabsf(x.y)) + (fabsf(x.z) + fabsf(x.w));
+                        *reinterpret_cast<float4*>(dst + c0 + i) = x;
+                    }
                 }
+                if (converts_v<kBF16>() && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
                 p.ws_lse[slot] = row_lse;
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -600,6 +660,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             const int qrow = un.q_tile[t] * kBM + row;
             if (qrow < p.S) p.lse[(size_t)un.bh * (size_t)p.S + (size_t)qrow] = row_lse;
             const uint32_t tO = tmem + lane_base + C::col_o(t);
+            float osum = 0.f;   // converted V: a value beyond fp16's range makes O (and this sum) not finite
 #pragma unroll 1
             for (int box = 0; box < C::kBoxes; ++box) {
                 // the staging box is free once the previous TMA store has read it
@@ -616,6 +677,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                         float a, b2;
                         ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
                                        a, b2);
+                        if constexpr (converts_v<kBF16>()) osum += fabsf(a) + fabsf(b2);
                         pk[i] = ptx::pack2<kBF16>(a, b2);
                     }
 #pragma unroll
@@ -637,6 +699,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                     ptx::bulk_commit();
                 }
             }
+            if (converts_v<kBF16>() && qrow < p.S && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
             FA_TRACE_EV(leader, kTrEpilogue, kEvEpiDone, t);
         }
     }
@@ -728,6 +791,56 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
 }
 
 // ---------------------------------------------------------------------------------
+// V converter (bf16 inputs; warps 14-15, and the epilogue warpgroup's warps 8-11
+// when the epilogue runs in the softmax warpgroups): each V tile, once it has
+// landed, is rewritten in place from bf16 to fp16 (element by element, so the
+// swizzled layout stays valid), made visible to the tensor core's reads
+// (fence.proxy.async) and announced on its slot's conversion barrier.  The walk
+// over units and key tiles is the loader's: K_j, then V_j, for every key tile
+// of every unit.  A value beyond fp16's range becomes infinite, so O does too;
+// the epilogues check O and record kSiteRangeV (no per-element check here).
+template <int D, bool kSplit, int kWarps>
+__device__ __forceinline__ void vconvert_role(const Params& p, const ptx::WaitCtx& wc, uint32_t smem_base,
+                                              uint32_t bars, int conv_tid)
+{
+    using C = Cfg<D>;
+    const int lane = threadIdx.x & 31;
+    uint32_t kv_count = 0;
+    for (int r = 0;; ++r) {
+        const Unit un = unit_at<kSplit>(r, p);
+        if (un.status == kUnitDone) break;
+        if (un.status == kUnitSkip) continue;
+        for (int j = un.j0; j < un.nmax; ++j) {
+            const uint32_t iv = kv_count + 1;   // K_j's entry, then V_j's
+            kv_count += 2;
+            bool ok;
+            if constexpr (C::kFullPairs) {
+                const uint32_t q = iv / 2u, b = kBarKVFull + q % C::kPairs;
+                ok = ptx::mbar_wait_warp(wc, bars + 8 * b, (q / C::kPairs) & 1u, kSiteLoad | 0x80u | b);
+            } else {
+                const uint32_t slot = iv % C::kSlots;
+                ok = ptx::mbar_wait_warp(wc, bars + 8 * (kBarKVFull + slot), (iv / C::kSlots) & 1u,
+                                         kSiteLoad | 0x80u | (kBarKVFull + slot));
+            }
+            if (!ok) return;
+            const uint32_t tile = smem_base + C::kOffKV + (iv % C::kSlots) * C::kTileBytes;
+#pragma unroll 2
+            for (uint32_t off = (uint32_t)conv_tid * 16u; off < (uint32_t)C::kTileBytes; off += 32u * kWarps * 16u) {
+                uint32_t w[4];
+                ptx::ld_shared_v4(tile + off, w);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    w[k] = ptx::pack2<false>(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+                ptx::st_shared_v4(tile + off, w[0], w[1], w[2], w[3]);
+            }
+            ptx::fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + 8 * (C::kBarVConv + iv % C::kSlots));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------
 // tcgen05 MMA issuer (one thread).
 template <int D, bool kBF16, bool kSplit, bool kDec>
 __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem, uint32_t smem_base,
@@ -735,7 +848,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
 {
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);   // Q, K both K-major
-    constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, kBF16, true);      // V is MN-major (D contiguous)
+    constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, p_is_bf16<kBF16>(), true);   // V MN-major (D contiguous)
     uint32_t ph_q = 0u, ph_ph = 0u, ph_p = 0u, ph_oe = 0u, ph_sf = 0u;   // phase bit of tile t at bit t
     uint32_t kv_count = 0;
     FA_TRACE_DECL;
@@ -750,6 +863,16 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             const uint32_t slot = idx % C::kSlots;
             return ptx::mbar_wait(wc, bars + 8 * (kBarKVFull + slot), (idx / C::kSlots) & 1u,
                                   kSiteMma | (kBarKVFull + slot));
+        }
+    };
+    // V_j converted to fp16 (bf16 inputs): the tile the P*V MMAs read
+    auto v_wait = [&](uint32_t idx) -> bool {
+        if constexpr (converts_v<kBF16>()) {
+            const uint32_t slot = idx % C::kSlots;
+            return ptx::mbar_wait(wc, bars + 8 * (C::kBarVConv + slot), (idx / C::kSlots) & 1u,
+                                  kSiteMma | (C::kBarVConv + slot));
+        } else {
+            return kv_wait(idx);
         }
     };
     // frees the pair of ring entries ending at `idx` (see Cfg): one commit
@@ -821,7 +944,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         kv_release(kvb);
         for (int j = un.j0; j < un.nmax; ++j) {
             const uint32_t iv = kvb + 2 * (j - un.j0) + 1, ik = iv + 1;
-            bool v_ready = C::kFullPairs, k_ready = false;
+            bool v_ready = C::kFullPairs && !converts_v<kBF16>(), k_ready = false;
             if constexpr (kDec) {
                 // the next scores first: QK_t(j+1) needs only S_t(j) read into the
                 // softmax's registers, so it runs while that softmax computes P_t(j)
@@ -860,7 +983,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                         ph_oe ^= 1u << t;
                     }
                     if (!v_ready) {
-                        if (!kv_wait(iv)) goto done;
+                        if (!v_wait(iv)) goto done;
                         v_ready = true;
                     }
                     ptx::tc_fence_after();
@@ -945,6 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kSlots; ++s) {
             ptx::mbar_init(bars + 8 * (kBarKVFull + s), C::kFullPairs ? 2 : 1);   // (K_j's and V_j's copies)
             ptx::mbar_init(bars + 8 * (C::kBarKVEmpty + s), 1);
+            ptx::mbar_init(bars + 8 * (C::kBarVConv + s), conv_warps<kBF16, kSplit>() > 0 ? conv_warps<kBF16, kSplit>() : 1);
         }
         ctl[1] = 0u;
         ptx::fence_mbar_init();
@@ -976,13 +1100,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         softmax_role<D, kBF16, kSplit, kDec>(p, wc, warp >> 2, tmem, bars, stats);
     } else if (warp < 12) {
         ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kEpilogue>();
-        correction_epilogue_role<D, kBF16, kSplit>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
+        if constexpr (conv_warps<kBF16, kSplit>() == 6)
+            vconvert_role<D, kSplit, 6>(p, wc, base, bars, threadIdx.x - 8 * 32);
+        else
+            correction_epilogue_role<D, kBF16, kSplit>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
     } else {
         ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kControl>();
         if (warp == 12) {
             if (lane == 0) load_role<D, kSplit>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {
             if (lane == 0) mma_role<D, kBF16, kSplit, kDec>(p, wc, tmem, base, bars);
+        } else if constexpr (conv_warps<kBF16, kSplit>() == 6) {
+            vconvert_role<D, kSplit, 6>(p, wc, base, bars, 128 + threadIdx.x - 14 * 32);
+        } else if constexpr (conv_warps<kBF16, kSplit>() == 2) {
+            vconvert_role<D, kSplit, 2>(p, wc, base, bars, threadIdx.x - 14 * 32);
         }
         __syncwarp();
     }

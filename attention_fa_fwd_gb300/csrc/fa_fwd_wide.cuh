@@ -33,9 +33,10 @@
 // moves only when the row maximum passes b + T; T = 15 for fp16, 30 for bf16,
 // as in the two-tile kernel), warp-wide as there; the softmax warps rescale O
 // in TMEM themselves ("G6", V44), each warpgroup its half of O's columns;
-// only then do they wait for the previous P*V to complete.  As in the two-tile
-// kernel, bf16 rows normalise O by l + dl, dl adding per step the rounding of
-// each half's largest p to bf16.
+// only then do they wait for the previous P*V to complete.  bf16 rows
+// normalise O by l + dl, dl adding per step the rounding of each half's
+// largest p to bf16 (as the two-tile kernel does).  This layout keeps P in
+// bf16 for bf16 inputs (no conversion of V).
 //
 // CTA layout (512 threads, one CTA per SM):
 //   warps 0-3   softmax, keys [0, BN/2) of each step

@@ -81,7 +81,9 @@ typedef enum {
     FA_ERR_MISALIGNED = 3,   /* a tensor pointer not 16-byte aligned */
     FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, copy, tensor map) */
     FA_ERR_TIMEOUT = 5,      /* a bounded in-kernel wait gave up (reported by fa_device_status) */
-    FA_ERR_SCRATCH = 6       /* fa_fwd_splitkv_static: the problem needs more than its static scratch */
+    FA_ERR_SCRATCH = 6,      /* fa_fwd_splitkv_static: the problem needs more than its static scratch */
+    FA_ERR_RANGE = 7         /* bf16 inputs: O came out not finite - V held an element beyond +-65504 (fp16's
+                                range) or an input was not finite (reported by fa_device_status) */
 } fa_status_t;
 
 /*
@@ -253,14 +255,20 @@ int fa_fwd_schedule_table(int B, int H, int S, int D, int causal, int dtype, int
                           int* n_ctas, int* n_units);
 
 /*
- * fa_device_status - status word of the bounded in-kernel waits.
+ * fa_device_status - the device status word of the kernels.
  *
  * Every wait inside the kernels gives up after a time limit (default 4 s,
  * FA_WAIT_TIMEOUT_MS overrides it when the library is loaded), records the
- * wait site in a device status word and makes its CTA exit cleanly.  This call
- * synchronises `stream`, reads the word, clears it if `clear` is non-zero and
- * returns FA_OK or FA_ERR_TIMEOUT; *site (if non-null) receives the recorded
- * site code (0 = none).  FA_ERR_CUDA if the synchronisation fails.
+ * wait site in a device status word and makes its CTA exit cleanly.  With
+ * bf16 inputs the two-tile layout computes P*V in fp16 (P and V of one type;
+ * bf16's 8-bit significand on P measurably moves O past the output's rounding
+ * midpoints on near one-hot rows), converting V to fp16 in shared memory: an
+ * element of V beyond +-65504 becomes infinite, and a CTA whose O comes out
+ * not finite records site 0x800.  This
+ * call synchronises `stream`, reads the word, clears it if `clear` is non-zero
+ * and returns FA_OK, FA_ERR_RANGE (site 0x800) or FA_ERR_TIMEOUT (any other
+ * site); *site (if non-null) receives the recorded site code (0 = none).
+ * FA_ERR_CUDA if the synchronisation fails.
  */
 int fa_device_status(cudaStream_t stream, int clear, unsigned int* site);
 

@@ -23,7 +23,7 @@ def test_exports_every_header_function(L):
 
 
 def test_strerror_every_status(L):
-    for code in range(6):
+    for code in range(8):
         assert fa.strerror(code) and fa.strerror(code) != "unknown status"
     assert fa.strerror(99) == "unknown status"
 

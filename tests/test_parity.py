@@ -212,3 +212,17 @@ def test_rejected_call_launches_nothing():
     assert (o == 7.0).all() and (lse == 7.0).all()
     with pytest.raises(ValueError):
         fa.fa_fwd(q.transpose(1, 2), k, v)
+
+
+def test_bf16_v_beyond_fp16_range_is_reported():
+    """bf16 inputs run P*V in fp16 (V converted in shared memory): an element of
+    V beyond +-65504 becomes infinite, O is not finite, and the status word
+    says the result is invalid; the next call on valid inputs reports nothing."""
+    q, k, v = make_qkv(1, 2, 256, 128, "bf16", seed=9)
+    v[0, 1, 100, 5] = 1.0e6
+    fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    status, site = fa.device_status(clear=True)
+    assert status == fa.FA_ERR_RANGE and site == 0x800
+    v[0, 1, 100, 5] = 65280.0           # the largest bf16 value within fp16's range (65504 rounds to 2^16)
+    fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    assert fa.device_status(clear=True) == (fa.FA_OK, 0)
