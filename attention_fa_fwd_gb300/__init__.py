@@ -22,7 +22,7 @@ from . import _build
 
 __all__ = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "splitkv_workspace_bytes", "fa_fwd_hostio", "launch_info", "plan", "schedule_table", "device_status",
            "selftest_wait_timeout", "selftest_exp2_poly", "strerror", "build", "lib", "header_functions",
-           "set_layout", "layout", "LAYOUT_AUTO", "LAYOUT_TWO_TILE", "LAYOUT_ONE_TILE",
+           "set_layout", "layout", "LAYOUT_AUTO", "LAYOUT_TWO_TILE", "LAYOUT_ONE_TILE", "debug_stats",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_SCRATCH", "FA_ERR_RANGE", "FaError"]
 
@@ -336,6 +336,52 @@ def device_status(clear: bool = True, stream=None) -> tuple[int, int]:
     if rc not in (FA_OK, FA_ERR_TIMEOUT, FA_ERR_RANGE):
         raise FaError(rc, "fa_device_status")
     return rc, site.value
+
+
+_dbg_lib = None
+
+
+def debug_stats(q, k, v, causal: bool = False, scale: float | None = None):
+    """One pass through the debug-statistics build of the library (a separate
+    .so, compiled on first use with -DFA_DEBUG_STATS), the debug mode of "CUDA
+    手写masked multi-head attention", section 6.3: each row hands its running
+    statistics to the host.  Returns (o, lse, stats, counts, rule): stats
+    [B, H, S, 2] float32 holds each row's final base b and row sum
+    l = sum 2^(x - b) (x the scaled score in base 2; ln2 * (b + log2 l) is the
+    LSE); counts = (warp rescales of O, row re-bases after a row's first key
+    tile); rule = (threshold T, overshoot) of the re-base rule for q's dtype."""
+    global _dbg_lib
+    B, H, S, D, scale, out, lse = _prepare(q, k, v, scale, None, None)
+    if _dbg_lib is None:
+        L = ctypes.CDLL(_build.build(debug_stats=True))
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_debug_stats_set.argtypes = [vp, vp]
+        L.fa_debug_rebase_rule.argtypes = [i, ctypes.POINTER(f), ctypes.POINTER(f)]
+        L.fa_device_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint)]
+        for name in ("fa_fwd", "fa_debug_stats_set", "fa_debug_rebase_rule", "fa_device_status"):
+            getattr(L, name).restype = i
+        _dbg_lib = L
+    L = _dbg_lib
+    stats = torch.full((B, H, S, 2), float("nan"), device=q.device, dtype=torch.float32)
+    counts = torch.zeros(2, device=q.device, dtype=torch.int64)
+    with _on_device(q.device):
+        stream = _stream_ptr(None)
+        rc = L.fa_debug_stats_set(stats.data_ptr(), counts.data_ptr())
+        if rc == FA_OK:
+            rc = L.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, S, D,
+                          int(bool(causal)), float(scale), _DTYPE[q.dtype], stream)
+        site = ctypes.c_uint(0)
+        st = L.fa_device_status(stream, 1, ctypes.byref(site))
+        L.fa_debug_stats_set(None, None)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd (debug statistics build)")
+    if st != FA_OK:
+        raise FaError(st, f"fa_fwd (debug statistics build), site {site.value:#x}")
+    t, o_ = ctypes.c_float(0), ctypes.c_float(0)
+    L.fa_debug_rebase_rule(_DTYPE[q.dtype], ctypes.byref(t), ctypes.byref(o_))
+    c = counts.cpu().tolist()
+    return out, lse, stats, (c[0], c[1]), (t.value, o_.value)
 
 
 def selftest_wait_timeout(timeout_us: int, stream=None) -> None:

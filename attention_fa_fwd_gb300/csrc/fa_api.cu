@@ -29,6 +29,11 @@ __device__ unsigned int g_fa_status = 0u;
 unsigned long long* g_trace = nullptr;
 int g_trace_ctas = 0, g_trace_cap = 0;
 #endif
+#ifdef FA_DEBUG_STATS
+// Side buffers of the FA_DEBUG_STATS build, set with fa_debug_stats_set.
+float* g_dbg_rows = nullptr;
+unsigned long long* g_dbg_count = nullptr;
+#endif
 
 constexpr int kMaxDevices = 64;
 
@@ -660,6 +665,12 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
     a.p.trace = nullptr;
     a.p.trace_ctas = 0;
     a.p.trace_cap = 0;
+    a.p.dbg_rows = nullptr;
+    a.p.dbg_count = nullptr;
+#ifdef FA_DEBUG_STATS
+    a.p.dbg_rows = g_dbg_rows;
+    a.p.dbg_count = g_dbg_count;
+#endif
 #ifdef FA_TRACE
     a.p.trace = g_trace;
     a.p.trace_ctas = g_trace_ctas;
@@ -901,6 +912,36 @@ int fa_selftest_exp2_poly(const float* x, float* y, int n, cudaStream_t stream)
     const int e = fa::launch_exp2_poly_selftest(x, y, n, stream);
     return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+#ifdef FA_DEBUG_STATS
+// Debug-statistics build only ("CUDA手写masked multi-head attention", 6.3: a
+// debug mode that hands each row's running maximum and sum to the host).  Every
+// later one-pass fa_fwd writes, per row (b*H + h, i), its final base b and row
+// sum l = sum over the row's keys of 2^(x - b), x the scaled score in base 2,
+// into rows ([B*H, S, 2] fp32, device, caller-owned), and adds to counters[0]
+// the warp rescales of O and to counters[1] the row re-bases after a row's
+// first key tile (device, 2 x u64, caller-owned, zeroed by the caller).  Both
+// null: off.  ln2 * (b + log2 l) is the row's LSE.
+int fa_debug_stats_set(float* rows, unsigned long long* counters)
+{
+    if ((rows == nullptr) != (counters == nullptr)) return FA_ERR_INVALID_ARG;
+    g_dbg_rows = rows;
+    g_dbg_count = counters;
+    return FA_OK;
+}
+
+// The re-base rule of P's type for `dtype` inputs: threshold T and overshoot,
+// both in base-2 units (a re-base happens when the tile maximum passes b + T
+// and moves b to the maximum plus the overshoot).
+int fa_debug_rebase_rule(int dtype, float* threshold, float* overshoot)
+{
+    if (!threshold || !overshoot || (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16)) return FA_ERR_INVALID_ARG;
+    const bool p_bf16 = dtype == FA_DTYPE_BF16 ? fa::p_is_bf16<true>() : fa::p_is_bf16<false>();
+    *threshold = p_bf16 ? fa::rebase_threshold<true>() : fa::rebase_threshold<false>();
+    *overshoot = p_bf16 ? fa::rebase_overshoot<true>() : fa::rebase_overshoot<false>();
+    return FA_OK;
+}
+#endif
 
 #ifdef FA_TRACE
 // Trace build only: every later fa_fwd records events of CTAs [0, ctas) into

@@ -49,6 +49,12 @@ struct Params {
     unsigned long long* trace;
     int trace_ctas;
     int trace_cap;
+    // Debug statistics (used only by the FA_DEBUG_STATS build; null otherwise):
+    // per row (b*H + h, i) its final base b and row sum l = sum 2^(x - b)
+    // ([B*H, S, 2] fp32), and two counters: warp rescales of O, row re-bases
+    // after a row's first key tile.
+    float* dbg_rows;
+    unsigned long long* dbg_count;
     // Table schedule (kSchedTable): CTA c runs units tab_unit[tab_off[c]] ..
     // tab_unit[tab_off[c + 1] - 1] in that order; a unit is bh * n_qgroups + qg.
     // Kept last: the kernel takes Params as a __grid_constant__ parameter and

@@ -461,6 +461,16 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             const float cand = fmaxf(b, mx);
             const bool rebase = cand > b + rebase_threshold<p_is_bf16<kBF16>()>();
             const bool rescale = j > un.j0 && __any_sync(0xffffffffu, rebase);
+#ifdef FA_DEBUG_STATS
+            if (p.dbg_count != nullptr && j > un.j0) {
+                // the debug build counts the kernel's own re-bases
+                const unsigned rows = __popc(__ballot_sync(0xffffffffu, rebase));
+                if (lane == 0 && rows > 0u) {
+                    atomicAdd(p.dbg_count + 0, 1ull);
+                    atomicAdd(p.dbg_count + 1, (unsigned long long)rows);
+                }
+            }
+#endif
             float h = 1.f;
             if (rebase || rescale) {
                 // a row that re-bases moves to its maximum plus the overshoot; a
@@ -536,6 +546,17 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), sa, sb);
             l = fmaf(l, h, sa + sb);
         }
+#ifdef FA_DEBUG_STATS
+        if (!kSplit && p.dbg_rows != nullptr) {
+            // the debug build writes each row's final base and row sum
+            const int qrow = q_tile * kBM + row;
+            if (qrow < p.S) {
+                float* d = p.dbg_rows + 2 * ((size_t)un.bh * p.S + qrow);
+                d[0] = b;
+                d[1] = l;
+            }
+        }
+#endif
         if constexpr (epi_in_softmax<kBF16, kSplit>()) {
             // this tile's epilogue, here: O_t is final once its last PV completed
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarOFull + t), ph_o, kSiteSoftmax | (kBarOFull + t))) return;

@@ -195,33 +195,36 @@ def time_oracle(w, q, k, v, budget_s: float, steps: int, seed: int = 0):
     return statistics.median(tflops), statistics.median(per_step), desc, nthreads
 
 
-# the kernel's re-base thresholds (log2 units) by input type
-KERNEL_REBASE_T = {"bf16": 30.0, "fp16": 15.0}
-
-
-def rescale_events(w, q, k, v, heads: int = 1):
-    """Re-bases counted by the oracle's lazy-rescale recurrence (row level, P
-    rounded to the input type) on the first `heads` heads at full length, for
-    the pages' threshold 8 and the kernel's, run side by side."""
+def rescale_events(w, q, k, v, heads: int = 1, fa=None):
+    """Re-bases of the lazy rescale: the kernel's own counts over the whole
+    workload (its debug-statistics build, one extra pass), and the oracle's
+    lazy-rescale recurrence (row level, P rounded to fp16, no overshoot) on the
+    first `heads` heads at the pages' threshold 8 and the kernel's T."""
     import oracle
     from fa_inputs import to_f64
     BH, S, D = w.B * w.H, w.S, w.D
+    kernel = None
+    T = 15.0
+    if fa is not None:
+        _, _, _, counts, (T, over) = fa.debug_stats(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, scale=w.scale)
+        kernel = {"heads": BH, "warp_rescales": counts[0], "row_rebases": counts[1],
+                  "rule": {"T": T, "overshoot": over}}
     qs, ks, vs = (to_f64(x.reshape(BH, S, D)[:heads].unsqueeze(0)) for x in (q, k, v))
     out = {}
 
     def run(t):
-        out[t] = oracle.attention_lazy(qs, ks, vs, w.causal, w.scale, 128, t, w.dtype, nthreads=heads)[2]
+        out[t] = oracle.attention_lazy(qs, ks, vs, w.causal, w.scale, 128, t, "fp16", nthreads=heads)[2]
 
-    ts = [8.0, KERNEL_REBASE_T[w.dtype]]
+    ts = [8.0, T]
     th = [threading.Thread(target=run, args=(t,)) for t in ts]
     for t in th:
         t.start()
     for t in th:
         t.join()
     steps = out[ts[0]]["steps"]
-    return {"model": "oracle lazy-rescale recurrence, row level", "heads": heads, "row_tile_steps": steps,
-            "row_rebases": {f"T={t:g}": out[t]["rebases"] for t in ts},
-            "kernel_T": KERNEL_REBASE_T[w.dtype]}
+    return {"kernel": kernel,
+            "model": {"what": "oracle lazy-rescale recurrence, row level, no overshoot", "heads": heads,
+                      "row_tile_steps": steps, "row_rebases": {f"T={t:g}": out[t]["rebases"] for t in ts}}}
 
 
 def aggregate(ms_local: float, flops_per_rank: float, world: int, dist=None, device=None):
@@ -454,7 +457,7 @@ def run_ours(args, w):
     elif not args.no_cpu_baseline:
         line["cpu_baseline"] = None
     if w.kind == "stress" and not args.no_cpu_baseline:
-        line["rescale"] = rescale_events(w, q, k, v)
+        line["rescale"] = rescale_events(w, q, k, v, fa=fa)
     if not args.no_per_config and world == 1:
         del qd, kd, vd, od, ld
         torch.cuda.empty_cache()
