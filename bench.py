@@ -281,10 +281,33 @@ def time_device_loop(step, stream, dev, steps):
     return e0.elapsed_time(e1) / steps
 
 
+L2_BYTES = 129 * 1000 * 1000   # GB300 L2
+
+
+def time_flushed_steps(step, flush, stream, dev, steps):
+    """Milliseconds per step with L2 flushed before every step: each step is
+    bracketed by its own pair of CUDA events on the launching stream, the
+    flush (a write of twice the L2's size) runs outside the pair."""
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for a, b in pairs:
+        flush()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    return statistics.fmean(a.elapsed_time(b) for a, b in pairs)
+
+
 def per_config_lines(fa, dev, local, stream, peak_burst, peak_sustained, target_s):
     """Device time, TFLOPS and fraction of peak of every workload, each timed
-    for about `target_s` seconds after a warm-up, with its own clock samples."""
+    for about `target_s` seconds after a warm-up, with its own clock samples.
+    Workloads whose tensors exceed the L2 run back to back; the others get an
+    L2 flush before every step (their back-to-back time, inputs resident in
+    L2, is reported beside it)."""
     out = {}
+    flush_buf = None
     for tag, name in PER_CONFIG:
         w = WORKLOADS[name]
         q, k, v = make_workload(w)
@@ -298,11 +321,24 @@ def per_config_lines(fa, dev, local, stream, peak_burst, peak_sustained, target_
         for _ in range(5):
             step()
         probe = time_device_loop(step, stream, dev, 10)
-        steps = int(min(200000, max(20, target_s * 1e3 / max(probe, 1e-3))))
+        resident = w.io_bytes() < L2_BYTES
+        warm = None
+        if resident:
+            if flush_buf is None:
+                flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+            flush = lambda: flush_buf.fill_(1)
+            warm = time_device_loop(step, stream, dev, int(min(20000, max(20, 0.1e3 / max(probe, 1e-3)))))
+            per_iter = time_flushed_steps(step, flush, stream, dev, 5) + 0.08   # + ~80 us of flush
+            steps = int(min(5000, max(20, target_s * 1e3 / per_iter)))
+        else:
+            steps = int(min(200000, max(20, target_s * 1e3 / max(probe, 1e-3))))
         sampler = ClockSampler(local)
         sampler.start()
         time.sleep(0.25)
-        ms = time_device_loop(step, stream, dev, steps)
+        if resident:
+            ms = time_flushed_steps(step, flush, stream, dev, steps)
+        else:
+            ms = time_device_loop(step, stream, dev, steps)
         clocks = sampler.stop()
         status, site = fa.device_status(clear=True, stream=stream)
         if status != fa.FA_OK:
@@ -312,9 +348,16 @@ def per_config_lines(fa, dev, local, stream, peak_burst, peak_sustained, target_
                      "dtype": w.dtype, "kind": w.kind, "steps": steps, "ms_per_step": round(ms, 6),
                      "tflops": round(tflops, 3), "frac_burst": round(tflops / peak_burst, 4),
                      "frac_sustained": round(tflops / peak_sustained, 4),
+                     "l2": ("L2 flushed before every step (tensors %.1f MB fit in L2)" % (w.io_bytes() / 1e6))
+                           if resident else ("tensors %.0f MB exceed the L2; back to back" % (w.io_bytes() / 1e6)),
                      "timed_s": round(ms * steps / 1e3, 3), "clocks": clocks}
+        if warm is not None:
+            out[name]["ms_per_step_l2_resident"] = round(warm, 6)
+            out[name]["tflops_l2_resident"] = round(w.flops() / (warm * 1e-3) / 1e12, 3)
         del qd, kd, vd, od, ld
         torch.cuda.empty_cache()
+    del flush_buf
+    torch.cuda.empty_cache()
     return out
 
 
