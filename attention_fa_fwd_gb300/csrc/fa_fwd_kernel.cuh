@@ -122,10 +122,10 @@ constexpr bool kEpilogueInSoftmax = FA_EPILOGUE_IN_SOFTMAX != 0;
 // epilogue warpgroup in the softmax warpgroups and all six warps converting
 // measured slower (train 1105 vs 1125, stress 1140 vs 1235 TFLOPS): the
 // conversion's cost is issue slots, not latency.
-template <bool kBF16, bool kSplit>
-__host__ __device__ constexpr bool epi_in_softmax() { return kEpilogueInSoftmax && !kSplit; }
-template <bool kBF16, bool kSplit>
-__host__ __device__ constexpr int conv_warps() { return converts_v<kBF16>() ? (epi_in_softmax<kBF16, kSplit>() ? 6 : 2) : 0; }
+template <bool kBF16, bool kSplit, bool kDec>
+__host__ __device__ constexpr bool epi_in_softmax() { return kEpilogueInSoftmax && !kSplit && !kDec; }
+template <bool kBF16, bool kSplit, bool kDec>
+__host__ __device__ constexpr int conv_warps() { return converts_v<kBF16>() ? (epi_in_softmax<kBF16, kSplit, kDec>() ? 6 : 2) : 0; }
 static_assert(kExp2PolyPairs >= 0 && kExp2PolyPairs <= 16, "FA_EXP2_POLY_PAIRS must be in [0, 16]");
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -142,6 +142,14 @@ template <bool kBF16> struct RegSplit<128, kBF16, true, false> {
 template <bool kBF16, bool kDec> struct RegSplit<64, kBF16, false, kDec> {
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72;
 };
+// key split (decoupled instances): a warpgroup holds 64 scores per row, and the
+// epilogue merges two accumulators
+template <bool kBF16> struct RegSplit<64, kBF16, false, true> {
+    static constexpr uint32_t kSoftmax = 168, kEpilogue = 104, kControl = 72;
+};
+template <bool kBF16> struct RegSplit<64, kBF16, true, true> {
+    static constexpr uint32_t kSoftmax = 168, kEpilogue = 104, kControl = 72;
+};
 template <int D, bool kBF16, bool kSplit, bool kDec>
 constexpr bool reg_split_fits()
 {
@@ -150,7 +158,7 @@ constexpr bool reg_split_fits()
 }
 static_assert(reg_split_fits<128, false, false, false>() && reg_split_fits<128, false, true, false>() &&
                   reg_split_fits<64, false, false, false>() && reg_split_fits<64, false, false, true>() &&
-                  reg_split_fits<64, false, true, false>(),
+                  reg_split_fits<64, false, true, false>() && reg_split_fits<64, false, true, true>(),
               "register split must add up to 512");
 
 // Barrier indices inside the barrier array.
@@ -206,11 +214,13 @@ struct Cfg {
     // TMEM columns of the score region S_t, the output accumulator O_t and P_t.
     // D=128 fills the 512 columns with S0 | S1 | O0 | O1, so P_t overwrites the
     // first half of S_t and the next QK_t must wait for PV_t.  D=64 leaves 128
-    // columns free: the decoupled instances (kDec, launched for one query tile
-    // per unit) give P_t its own 64 there, so QK_t(j+1) can run as soon as the
-    // softmax has read S_t(j), while P_t(j) waits for its PV.  With two tiles
-    // per unit P_t stays on S_t: the tiles alternate anyway, and the decoupled
-    // order measured 4-6% slower there (10x64x1024x64).
+    // columns free.  The decoupled instances (kDec, launched for one query tile
+    // per unit) use S0 for the tile's scores, columns 384-447 for its P and
+    // O0 | O1 for two accumulators: warpgroup h takes keys 64h..64h+63 of every
+    // key tile (scores S0[64h..], P at 384 + 32h, accumulator O_h), so QK(j+1)
+    // can run as soon as both warpgroups have read S(j), while P_h(j) waits for
+    // its PV.  With two tiles per unit P_t stays on S_t: the tiles alternate
+    // anyway, and a decoupled order measured 4-6% slower there (10x64x1024x64).
     static constexpr bool kSepP = (D == 64);
     __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
     __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
@@ -375,13 +385,21 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
     const int wq = (threadIdx.x >> 5) & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_base + C::col_s(t);
+    const uint32_t tS = tmem + lane_base + (kDec ? C::col_s(0) + 64u * t : C::col_s(t));
     const uint32_t tO = tmem + lane_base + C::col_o(t);
     // decoupled order (separate P): the next QK_t runs before PV_t, so P_t and
     // O_t wait for that PV explicitly; in the shared order S_t(j) implies that
     // PV_t(j-1) has finished
     static_assert(!kDec || C::kSepP, "the decoupled order needs P in its own columns");
-    const uint32_t tP = tmem + lane_base + C::col_p(t, kDec);
+    // Decoupled instances run one query tile per unit and split each key tile
+    // between the two warpgroups (keys 0-63 and 64-127 of every step): each
+    // keeps its own base, row sum and O accumulator (O_t), and the epilogue
+    // merges the two halves.  So a key step's softmax work per warpgroup halves
+    // and no row maximum is exchanged.
+    constexpr bool kKS = kDec;
+    constexpr int kCols = kKS ? 64 : 128;      // S columns this warpgroup reads per key step
+    constexpr int kChunks = kCols / 32;
+    const uint32_t tP = tmem + lane_base + (kKS ? C::col_p(0, true) + 32u * t : C::col_p(t, kDec));
     const float sl2 = p.scale_log2;
     uint32_t ph_s = 0, ph_te = 0, ph_o = 0;
     uint32_t n_pub = 0;   // separate P: P tiles this warpgroup published (one PV each)
@@ -393,10 +411,11 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         // t is a runtime value: select instead of indexing, so the unit stays in registers
-        const int nkv = t ? un.nkv[1] : un.nkv[0];
-        const int q_tile = t ? un.q_tile[1] : un.q_tile[0];
+        const int tt = kKS ? 0 : t;   // the query tile this warpgroup works on
+        const int nkv = tt ? un.nkv[1] : un.nkv[0];
+        const int q_tile = tt ? un.q_tile[1] : un.q_tile[0];
         // the masked tile: the row's last key tile (always nkv - 1 without a split)
-        const int last = kSplit ? (t ? un.last[1] : un.last[0]) : nkv - 1;
+        const int last = kSplit ? (tt ? un.last[1] : un.last[0]) : nkv - 1;
         if (nkv == 0) continue;
         float b = -INFINITY;   // base of the row, base-2 scaled units
         float l = 0.f;         // running sum of 2^(x - b): gives the LSE
@@ -409,20 +428,21 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
         // 1.1e-3 off).  fp16 inputs round O to 2^-11 relative: dl stays 0.
         float dl = 0.f;
         for (int j = un.j0; j < nkv; ++j) {
-            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + t), ph_s, kSiteSoftmax | (kBarSFull + t))) return;
+            // (key split: both warpgroups read the one tile's scores, committed on SFull_0)
+            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + tt), ph_s, kSiteSoftmax | (kBarSFull + tt))) return;
             ph_s ^= 1u;
             FA_TRACE_EV(tr, t, kEvSReady, j);
             ptx::tc_fence_after();
             // scores of the row; each 32-column load also returns its maximum
-            uint32_t sr[128];
-            float pm[4];
+            uint32_t sr[kCols];
+            float pm[kChunks];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) ptx::tmem_ld32_max(tS + 32 * c, sr + 32 * c, pm[c]);
+            for (int c = 0; c < kChunks; ++c) ptx::tmem_ld32_max(tS + 32 * c, sr + 32 * c, pm[c]);
             ptx::tmem_wait_ld();
             ptx::reg_fence(sr);
             ptx::reg_fence(pm);
             if constexpr (kDec) {
-                // S_t is in registers: the MMA issuer may compute the next S_t now
+                // S is in registers: once both warpgroups are here the MMA issuer may compute the next S
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarSFree + t));
@@ -435,22 +455,25 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 const int qrow = q_tile * kBM + row;
                 int lim = p.S - 1 - j * kBN;
                 if (p.causal) lim = min(lim, qrow - j * kBN);
+                if (kKS) lim -= 64 * t;   // this warpgroup's first key of the tile
 #pragma unroll
-                for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
-                // maximum over what is left: four chains of three-input max
-                float m[4];
+                for (int c = 0; c < kCols; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+                // maximum over what is left: one chain of three-input max per 32 columns
+                float m[kChunks];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) m[k] = ptx::max3(s[32 * k], s[32 * k + 1], s[32 * k + 2]);
+                for (int k = 0; k < kChunks; ++k) m[k] = ptx::max3(s[32 * k], s[32 * k + 1], s[32 * k + 2]);
 #pragma unroll
                 for (int i = 3; i < 31; i += 2) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) m[k] = ptx::max3(m[k], s[32 * k + i], s[32 * k + i + 1]);
+                    for (int k = 0; k < kChunks; ++k) m[k] = ptx::max3(m[k], s[32 * k + i], s[32 * k + i + 1]);
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], s[32 * k + 31]);
-                mraw = fmaxf(ptx::max3(m[0], m[1], m[2]), m[3]);
+                for (int k = 0; k < kChunks; ++k) m[k] = fmaxf(m[k], s[32 * k + 31]);
+                if constexpr (kKS) mraw = fmaxf(m[0], m[1]);
+                else mraw = fmaxf(ptx::max3(m[0], m[1], m[2]), m[3]);
             } else {
-                mraw = fmaxf(ptx::max3(pm[0], pm[1], pm[2]), pm[3]);
+                if constexpr (kKS) mraw = fmaxf(pm[0], pm[1]);
+                else mraw = fmaxf(ptx::max3(pm[0], pm[1], pm[2]), pm[3]);
             }
             const float mx = mraw * sl2;
             // conditional re-base: keep b unless the maximum passed b + T.  The O
@@ -484,7 +507,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             FA_TRACE_EV(tr, t, kEvMaxDone, j);
             if constexpr (kDec) {
                 // P_t and O_t are free once the PV of the previously published P_t
-                // completed (in this order S_t(j) does not imply it)
+                // completed (in this order S(j) does not imply it)
                 if (n_pub > 0 && !ptx::mbar_wait_warp(wc, bars + 8 * (kBarPVDone + t), (n_pub - 1) & 1u,
                                                       kSiteSoftmax | (kBarPVDone + t)))
                     return;
@@ -515,7 +538,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 dl = fmaf(dl, h, ptx::round16<p_is_bf16<kBF16>()>(pm) - pm);
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -533,11 +556,13 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 }
                 ptx::tmem_st16(tP + c * 16, pk);
                 if (c == 1 || c == 3) {
-                    // publish P (and, at c == 1, the rescaled O) for the MMA issuer
+                    // publish P (and, at c == 1, the rescaled O) for the MMA issuer;
+                    // a key-split warpgroup publishes its 64 keys once, on PFull
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bars + 8 * (c == 1 ? kBarPHalf + t : kBarPFull + t));
+                    if (lane == 0)
+                        ptx::mbar_arrive(bars + 8 * ((c == 1 && !kKS) ? kBarPHalf + t : kBarPFull + t));
                     if (c == 1) FA_TRACE_EV(tr, t, kEvExpDone, j);
                 }
             }
@@ -547,7 +572,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             l = fmaf(l, h, sa + sb);
         }
 #ifdef FA_DEBUG_STATS
-        if (!kSplit && p.dbg_rows != nullptr) {
+        if (!kSplit && !kKS && p.dbg_rows != nullptr) {
             // the debug build writes each row's final base and row sum
             const int qrow = q_tile * kBM + row;
             if (qrow < p.S) {
@@ -557,7 +582,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             }
         }
 #endif
-        if constexpr (epi_in_softmax<kBF16, kSplit>()) {
+        if constexpr (epi_in_softmax<kBF16, kSplit, kDec>()) {
             // this tile's epilogue, here: O_t is final once its last PV completed
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarOFull + t), ph_o, kSiteSoftmax | (kBarOFull + t))) return;
             ph_o ^= 1u;
@@ -607,7 +632,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
 // ---------------------------------------------------------------------------------
 // Correction/epilogue warpgroup: per unit and query tile, the final correction
 // O_t / l, the LSE, conversion to 16 bits, shared-memory staging, TMA store.
-template <int D, bool kBF16, bool kSplit>
+template <int D, bool kBF16, bool kSplit, bool kDec>
 __device__ __forceinline__ void correction_epilogue_role(const Params& p, const ptx::WaitCtx& wc,
                                                          const CUtensorMap* tm_o, uint32_t tmem, uint32_t smem_base,
                                                          uint32_t bars, const float4* stats, volatile uint32_t* ctl_go)
@@ -622,12 +647,130 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
     volatile uint32_t* go = ctl_go;   // leader's wait outcome, read by all 128 threads
     uint32_t ph_o = 0u, ph_t = 0u;   // phase bit of tile t at bit t
     FA_TRACE_DECL;
-    if constexpr (epi_in_softmax<kBF16, kSplit>()) return;   // the softmax warpgroups run the epilogue
+    if constexpr (epi_in_softmax<kBF16, kSplit, kDec>()) return;   // the softmax warpgroups run the epilogue
 
     for (int r = 0;; ++r) {
         const Unit un = unit_at<kSplit>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
+        if constexpr (kDec) {
+            // key split: the unit's one query tile has two partial results, keys
+            // 0-63 (O_0, base b0, sum l0) and 64-127 (O_1, b1, l1) of every key
+            // tile; with m = max(b0, b1) and w_h = 2^(b_h - m) the row's sum is
+            // w0 l0 + w1 l1 and its O is (w0 O_0 + w1 O_1) / (w0 l0' + w1 l1')
+            // (l' the normaliser, l + dl)
+            if (un.nkv[0] == 0) continue;
+            if (leader) {
+                bool ok = true;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    ok = ok &&
+                         ptx::mbar_wait(wc, bars + 8 * (kBarOFull + h), ph_o & 1u, kSiteEpilogue | (kBarOFull + h)) &&
+                         ptx::mbar_wait(wc, bars + 8 * (kBarStFull + h), ph_t & 1u, kSiteEpilogue | (kBarStFull + h));
+                go[0] = ok ? 1u : 0u;
+            }
+            ptx::named_bar_sync(1, 128);
+            if (go[0] == 0u) goto done;
+            ph_o ^= 1u;
+            ph_t ^= 1u;
+            ptx::tc_fence_after();
+            const float4 s0 = stats[row], s1 = stats[kBM + row];
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(bars + 8 * kBarStEmpty);
+                ptx::mbar_arrive(bars + 8 * (kBarStEmpty + 1));
+            }
+            const float m = fmaxf(s0.y, s1.y);   // b0 is finite: key 0 of every unit is unmasked
+            const float w0 = ptx::ex2(s0.y - m), w1 = ptx::ex2(s1.y - m);
+            const float lsum = w0 * s0.x + w1 * s1.x;
+            const float inv_l = 1.0f / (w0 * s0.z + w1 * s1.z);
+            const float c0 = w0 * inv_l, c1 = w1 * inv_l;
+            const float row_lse = (m + ptx::lg2(lsum)) * kLn2;
+            const uint32_t tO0 = tmem + lane_base + C::col_o(0), tO1 = tmem + lane_base + C::col_o(1);
+            static_assert(D == 64, "key split: D=64");
+            float osum = 0.f;   // converted V: a value beyond fp16's range makes O (and this sum) not finite
+            if constexpr (kSplit) {
+                const size_t slot = (size_t)un.id * kBM + row;   // one tile per unit
+                float* dst = p.ws_o + slot * D;
+#pragma unroll 1
+                for (int c0c = 0; c0c < D; c0c += 32) {
+                    uint32_t oa[32], ob[32];
+                    ptx::tmem_ld32(tO0 + c0c, oa);
+                    ptx::tmem_ld32(tO1 + c0c, ob);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence(oa);
+                    ptx::reg_fence(ob);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        float x[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            x[e] = fmaf(__uint_as_float(oa[i + e]), c0, __uint_as_float(ob[i + e]) * c1);
+                        if constexpr (converts_v<kBF16>()) osum += (fabsf(x[0]) + fabsf(x[1])) + (fabsf(x[2]) + fabsf(x[3]));
+                        *reinterpret_cast<float4*>(dst + c0c + i) = make_float4(x[0], x[1], x[2], x[3]);
+                    }
+                }
+                if (converts_v<kBF16>() && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
+                p.ws_lse[slot] = row_lse;
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(bars + 8 * kBarOEmpty);
+                    ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1));
+                }
+                continue;
+            }
+            const int qrow = un.q_tile[0] * kBM + row;
+            if (qrow < p.S) p.lse[(size_t)un.bh * (size_t)p.S + (size_t)qrow] = row_lse;
+#ifdef FA_DEBUG_STATS
+            if (p.dbg_rows != nullptr && qrow < p.S) {
+                // the debug build's per-row base and sum: the merged ones
+                float* d = p.dbg_rows + 2 * ((size_t)un.bh * p.S + qrow);
+                d[0] = m;
+                d[1] = lsum;
+            }
+#endif
+            // the staging box is free once the previous TMA store has read it
+            if (leader) ptx::bulk_wait_read0();
+            ptx::named_bar_sync(1, 128);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t oa[32], ob[32];
+                ptx::tmem_ld32(tO0 + half * 32, oa);
+                ptx::tmem_ld32(tO1 + half * 32, ob);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence(oa);
+                ptx::reg_fence(ob);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a = fmaf(__uint_as_float(oa[2 * i]), c0, __uint_as_float(ob[2 * i]) * c1);
+                    const float b2 = fmaf(__uint_as_float(oa[2 * i + 1]), c0, __uint_as_float(ob[2 * i + 1]) * c1);
+                    if constexpr (converts_v<kBF16>()) osum += fabsf(a) + fabsf(b2);
+                    pk[i] = ptx::pack2<kBF16>(a, b2);
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int chunk = half * 4 + cc;   // 16-byte chunk of the 128-byte row
+                    const uint32_t addr = stage + row * 128 + ((chunk ^ (row & 7)) << 4);
+                    ptx::st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(bars + 8 * kBarOEmpty);
+                ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1));
+            }
+            ptx::fence_proxy_async_shared();
+            ptx::named_bar_sync(1, 128);
+            if (leader) {
+                ptx::tma_store_3d(tm_o, stage, 0, un.q_tile[0] * kBM, un.bh);
+                ptx::bulk_commit();
+            }
+            if (converts_v<kBF16>() && qrow < p.S && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
+            continue;
+        }
         // one named barrier carries the leader's wait outcome to all 128
         // threads, so the warpgroup never splits over an abort
 #pragma unroll
@@ -873,7 +1016,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);   // Q, K both K-major
     constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, p_is_bf16<kBF16>(), true);   // V MN-major (D contiguous)
-    uint32_t ph_q = 0u, ph_ph = 0u, ph_p = 0u, ph_oe = 0u, ph_sf = 0u;   // phase bit of tile t at bit t
+    static_assert(!kDec, "the decoupled instances issue from mma_role_ks");
+    uint32_t ph_q = 0u, ph_ph = 0u, ph_p = 0u, ph_oe = 0u;   // phase bit of tile t at bit t
     uint32_t kv_count = 0;
     FA_TRACE_DECL;
 
@@ -949,12 +1093,6 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             if (un.nkv[t] == 0) continue;
             if (!ptx::mbar_wait(wc, bars + 8 * (kBarQFull + t), (ph_q >> t) & 1u, kSiteMma | (kBarQFull + t))) goto done;
             ph_q ^= 1u << t;
-            if constexpr (kDec) {
-                // S_t is overwritten: the softmax must have read the previous one
-                if (!ptx::mbar_wait(wc, bars + 8 * (kBarSFree + t), ((ph_sf >> t) & 1u) ^ 1u, kSiteMma | (kBarSFree + t)))
-                    goto done;
-                ph_sf ^= 1u << t;
-            }
             if (!k_in) {
                 if (!kv_wait(kvb)) goto done;
                 k_in = true;
@@ -969,29 +1107,6 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         for (int j = un.j0; j < un.nmax; ++j) {
             const uint32_t iv = kvb + 2 * (j - un.j0) + 1, ik = iv + 1;
             bool v_ready = C::kFullPairs && !converts_v<kBF16>(), k_ready = false;
-            if constexpr (kDec) {
-                // the next scores first: QK_t(j+1) needs only S_t(j) read into the
-                // softmax's registers, so it runs while that softmax computes P_t(j)
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (j + 1 < un.nkv[t]) {
-                        if (!ptx::mbar_wait(wc, bars + 8 * (kBarSFree + t), ((ph_sf >> t) & 1u) ^ 1u,
-                                            kSiteMma | (kBarSFree + t)))
-                            goto done;
-                        ph_sf ^= 1u << t;
-                        if (!k_ready) {
-                            if (!kv_wait(ik)) goto done;
-                            k_ready = true;
-                        }
-                        ptx::tc_fence_after();
-                        FA_TRACE_EV(true, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
-                        issue_qk(t, ik);
-                        ptx::mma_commit(bars + 8 * (kBarSFull + t));
-                        FA_TRACE_EV(true, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
-                        if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
-                    }
-                }
-            }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (j < un.nkv[t]) {
@@ -1020,22 +1135,19 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     ptx::tc_fence_after();
                     issue_pv(t, iv, 1, true);
                     FA_TRACE_EV(true, kTrMma, kEvPV, ((uint32_t)t << 12) | j);
-                    if constexpr (kDec) ptx::mma_commit(bars + 8 * (kBarPVDone + t));   // P_t may be rewritten
                     if (j == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarOFull + t));
                 }
-                if constexpr (!kDec) {
-                    if (j + 1 < un.nkv[t]) {
-                        if (!k_ready) {
-                            if (!kv_wait(ik)) goto done;
-                            k_ready = true;
-                            ptx::tc_fence_after();
-                        }
-                        FA_TRACE_EV(true, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
-                        issue_qk(t, ik);
-                        ptx::mma_commit(bars + 8 * (kBarSFull + t));
-                        FA_TRACE_EV(true, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
-                        if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
+                if (j + 1 < un.nkv[t]) {
+                    if (!k_ready) {
+                        if (!kv_wait(ik)) goto done;
+                        k_ready = true;
+                        ptx::tc_fence_after();
                     }
+                    FA_TRACE_EV(true, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
+                    issue_qk(t, ik);
+                    ptx::mma_commit(bars + 8 * (kBarSFull + t));
+                    FA_TRACE_EV(true, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
+                    if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
                 }
             }
             // V_j and K_{j+1} together; a unit's last V goes with the next
@@ -1046,6 +1158,130 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     }
 done:
     // every MMA must be complete before tensor memory is released
+    ptx::mma_commit(bars + 8 * kBarDrain);
+    ptx::mbar_wait_drain(wc, bars + 8 * kBarDrain, 0u, kSiteDrain | kBarDrain);
+}
+
+// ---------------------------------------------------------------------------------
+// MMA issuer of the decoupled, key-split instances (one query tile per unit,
+// D=64): per key step j, QK(j+1) into S as soon as both warpgroups have read
+// S(j) (SFree_0, SFree_1), then PV_h(j) for each key half h once warpgroup h
+// has published its P: O_h += P[:, 64h .. 64h+63] V[64h .. 64h+63, :], four
+// K=16 MMAs from P_h's 32 TMEM columns.  Each PV_h commits PVDone_h (P_h and
+// O_h may then be rewritten).
+template <int D, bool kBF16, bool kSplit>
+__device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem, uint32_t smem_base,
+                                            uint32_t bars)
+{
+    using C = Cfg<D>;
+    static_assert(C::kSepP && C::kFullPairs, "key split: D=64 layout");
+    constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);
+    constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, p_is_bf16<kBF16>(), true);
+    constexpr uint32_t kDescHi = ptx::sdesc_hi_sw128(1024);
+    uint32_t ph_q = 0u, ph_p = 0u, ph_oe = 0u, ph_sf = 0u;   // ph_p, ph_oe, ph_sf: bit h per key half
+    uint32_t kv_count = 0;
+    FA_TRACE_DECL;
+    // K_j and V_j land on one barrier at D=64: the wait for K_j also covers V_j
+    auto kv_wait = [&](uint32_t idx) -> bool {
+        const uint32_t q = idx / 2u, b = kBarKVFull + q % C::kPairs;
+        return ptx::mbar_wait(wc, bars + 8 * b, (q / C::kPairs) & 1u, kSiteMma | b);
+    };
+    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs)); };
+    auto s_free = [&]() -> bool {   // both warpgroups read the previous S
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (!ptx::mbar_wait(wc, bars + 8 * (kBarSFree + h), ((ph_sf >> h) & 1u) ^ 1u, kSiteMma | (kBarSFree + h)))
+                return false;
+            ph_sf ^= 1u << h;
+        }
+        return true;
+    };
+    const uint32_t qa = ptx::sdesc_lo(smem_base + C::kOffQ, 16);
+    auto issue_qk = [&](uint32_t idx) {
+        const uint32_t kb = ptx::sdesc_lo(smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes, 16);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            ptx::mma_ss(tmem + C::col_s(0), ptx::sdesc_join(qa + off, kDescHi), ptx::sdesc_join(kb + off, kDescHi),
+                        kIdescQK, kk > 0 ? 1u : 0u);
+        }
+    };
+    auto issue_pv = [&](int h, uint32_t idx, bool acc) {
+        const uint32_t vl = ptx::sdesc_lo(smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes, C::kBoxBytes);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = h * 4 + k4;   // key rows 16kk .. 16kk+15 of the tile
+            ptx::mma_ts(tmem + C::col_o(h), tmem + C::col_p(0, true) + kk * 8,
+                        ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || k4 > 0) ? 1u : 0u);
+        }
+    };
+    auto v_wait = [&](uint32_t idx) -> bool {   // V_j converted (bf16 inputs)
+        if constexpr (converts_v<kBF16>()) {
+            const uint32_t slot = idx % C::kSlots;
+            return ptx::mbar_wait(wc, bars + 8 * (C::kBarVConv + slot), (idx / C::kSlots) & 1u,
+                                  kSiteMma | (C::kBarVConv + slot));
+        } else {
+            return true;
+        }
+    };
+
+    for (int r = 0;; ++r) {
+        const Unit un = unit_at<kSplit>(r, p);
+        if (un.status == kUnitDone) break;
+        if (un.status == kUnitSkip) continue;
+        const uint32_t kvb = kv_count;
+        const int nkv = un.nkv[0];
+        FA_TRACE_EV(true, kTrMma, kEvUnit, un.id);
+        if (nkv > un.j0) {
+            if (!ptx::mbar_wait(wc, bars + 8 * kBarQFull, ph_q, kSiteMma | kBarQFull)) goto done;
+            ph_q ^= 1u;
+            if (!s_free() || !kv_wait(kvb)) goto done;
+            ptx::tc_fence_after();
+            issue_qk(kvb);
+            ptx::mma_commit(bars + 8 * kBarSFull);
+            FA_TRACE_EV(true, kTrMma, kEvQK, un.j0);
+            if (nkv == un.j0 + 1) ptx::mma_commit(bars + 8 * kBarQEmpty);
+        }
+        kv_release(kvb);
+        for (int j = un.j0; j < un.nmax; ++j) {
+            const uint32_t iv = kvb + 2 * (j - un.j0) + 1, ik = iv + 1;
+            if (j + 1 < nkv) {
+                if (!s_free() || !kv_wait(ik)) goto done;
+                ptx::tc_fence_after();
+                FA_TRACE_EV(true, kTrMma, kEvQKGo, j + 1);
+                issue_qk(ik);
+                ptx::mma_commit(bars + 8 * kBarSFull);
+                FA_TRACE_EV(true, kTrMma, kEvQK, j + 1);
+                if (j + 1 == nkv - 1) ptx::mma_commit(bars + 8 * kBarQEmpty);
+            }
+            if (j < nkv) {
+                if (!v_wait(iv)) goto done;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    FA_TRACE_EV(true, kTrMma, kEvPWait, ((uint32_t)h << 12) | j);
+                    if (!ptx::mbar_wait(wc, bars + 8 * (kBarPFull + h), (ph_p >> h) & 1u, kSiteMma | (kBarPFull + h)))
+                        goto done;
+                    ph_p ^= 1u << h;
+                    if (j == un.j0) {
+                        // O_h is overwritten: the previous unit's epilogue must have read it
+                        if (!ptx::mbar_wait(wc, bars + 8 * (kBarOEmpty + h), ((ph_oe >> h) & 1u) ^ 1u,
+                                            kSiteMma | (kBarOEmpty + h)))
+                            goto done;
+                        ph_oe ^= 1u << h;
+                    }
+                    ptx::tc_fence_after();
+                    FA_TRACE_EV(true, kTrMma, kEvPVGo, ((uint32_t)h << 12) | j);
+                    issue_pv(h, iv, j > un.j0);
+                    FA_TRACE_EV(true, kTrMma, kEvPV, ((uint32_t)h << 12) | j);
+                    ptx::mma_commit(bars + 8 * (kBarPVDone + h));   // P_h, O_h may be rewritten
+                    if (j == nkv - 1) ptx::mma_commit(bars + 8 * (kBarOFull + h));
+                }
+            }
+            if (j + 1 < un.nmax) kv_release(ik);
+        }
+        kv_count = kvb + 2 * (un.nmax - un.j0);
+    }
+done:
     ptx::mma_commit(bars + 8 * kBarDrain);
     ptx::mbar_wait_drain(wc, bars + 8 * kBarDrain, 0u, kSiteDrain | kBarDrain);
 }
@@ -1092,7 +1328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kSlots; ++s) {
             ptx::mbar_init(bars + 8 * (kBarKVFull + s), C::kFullPairs ? 2 : 1);   // (K_j's and V_j's copies)
             ptx::mbar_init(bars + 8 * (C::kBarKVEmpty + s), 1);
-            ptx::mbar_init(bars + 8 * (C::kBarVConv + s), conv_warps<kBF16, kSplit>() > 0 ? conv_warps<kBF16, kSplit>() : 1);
+            ptx::mbar_init(bars + 8 * (C::kBarVConv + s), conv_warps<kBF16, kSplit, kDec>() > 0 ? conv_warps<kBF16, kSplit, kDec>() : 1);
         }
         ctl[1] = 0u;
         ptx::fence_mbar_init();
@@ -1124,19 +1360,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         softmax_role<D, kBF16, kSplit, kDec>(p, wc, warp >> 2, tmem, bars, stats);
     } else if (warp < 12) {
         ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kEpilogue>();
-        if constexpr (conv_warps<kBF16, kSplit>() == 6)
+        if constexpr (conv_warps<kBF16, kSplit, kDec>() == 6)
             vconvert_role<D, kSplit, 6>(p, wc, base, bars, threadIdx.x - 8 * 32);
         else
-            correction_epilogue_role<D, kBF16, kSplit>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
+            correction_epilogue_role<D, kBF16, kSplit, kDec>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
     } else {
         ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kControl>();
         if (warp == 12) {
             if (lane == 0) load_role<D, kSplit>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {
-            if (lane == 0) mma_role<D, kBF16, kSplit, kDec>(p, wc, tmem, base, bars);
-        } else if constexpr (conv_warps<kBF16, kSplit>() == 6) {
+            if (lane == 0) {
+                if constexpr (kDec) mma_role_ks<D, kBF16, kSplit>(p, wc, tmem, base, bars);
+                else mma_role<D, kBF16, kSplit, kDec>(p, wc, tmem, base, bars);
+            }
+        } else if constexpr (conv_warps<kBF16, kSplit, kDec>() == 6) {
             vconvert_role<D, kSplit, 6>(p, wc, base, bars, 128 + threadIdx.x - 14 * 32);
-        } else if constexpr (conv_warps<kBF16, kSplit>() == 2) {
+        } else if constexpr (conv_warps<kBF16, kSplit, kDec>() == 2) {
             vconvert_role<D, kSplit, 2>(p, wc, base, bars, threadIdx.x - 14 * 32);
         }
         __syncwarp();
