@@ -445,7 +445,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 // S is in registers: once both warpgroups are here the MMA issuer may compute the next S
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarSFree + t));
+                ptx::mbar_arrive(bars + 8 * (kBarSFree + t), lane == 0);
             }
             FA_TRACE_EV(tr, t, kEvSLoaded, j);
             float* s = reinterpret_cast<float*>(sr);
@@ -561,8 +561,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(bars + 8 * ((c == 1 && !kKS) ? kBarPHalf + t : kBarPFull + t));
+                    ptx::mbar_arrive(bars + 8 * ((c == 1 && !kKS) ? kBarPHalf + t : kBarPFull + t), lane == 0);
                     if (c == 1) FA_TRACE_EV(tr, t, kEvExpDone, j);
                 }
             }
@@ -616,7 +615,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             if (converts_v<kBF16>() && in && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t));
+            ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t), lane == 0);
         } else {
             // hand (l, b) of every row to the epilogue
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarStEmpty + t), ph_te ^ 1u, kSiteSoftmax | (kBarStEmpty + t)))
@@ -624,7 +623,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             ph_te ^= 1u;
             stats[t * kBM + row] = make_float4(l, b, l + dl, 0.f);
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarStFull + t));
+            ptx::mbar_arrive(bars + 8 * (kBarStFull + t), lane == 0);
         }
     }
 }
@@ -660,14 +659,15 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             // w0 l0 + w1 l1 and its O is (w0 O_0 + w1 O_1) / (w0 l0' + w1 l1')
             // (l' the normaliser, l + dl)
             if (un.nkv[0] == 0) continue;
-            if (leader) {
+            if (wq == 0) {   // the leader's warp waits, all lanes together
                 bool ok = true;
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
                     ok = ok &&
                          ptx::mbar_wait(wc, bars + 8 * (kBarOFull + h), ph_o & 1u, kSiteEpilogue | (kBarOFull + h)) &&
                          ptx::mbar_wait(wc, bars + 8 * (kBarStFull + h), ph_t & 1u, kSiteEpilogue | (kBarStFull + h));
-                go[0] = ok ? 1u : 0u;
+                ok = __all_sync(0xffffffffu, ok);
+                if (leader) go[0] = ok ? 1u : 0u;
             }
             ptx::named_bar_sync(1, 128);
             if (go[0] == 0u) goto done;
@@ -676,10 +676,8 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             ptx::tc_fence_after();
             const float4 s0 = stats[row], s1 = stats[kBM + row];
             __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(bars + 8 * kBarStEmpty);
-                ptx::mbar_arrive(bars + 8 * (kBarStEmpty + 1));
-            }
+            ptx::mbar_arrive(bars + 8 * kBarStEmpty, lane == 0);
+            ptx::mbar_arrive(bars + 8 * (kBarStEmpty + 1), lane == 0);
             const float m = fmaxf(s0.y, s1.y);   // b0 is finite: key 0 of every unit is unmasked
             const float w0 = ptx::ex2(s0.y - m), w1 = ptx::ex2(s1.y - m);
             const float lsum = w0 * s0.x + w1 * s1.x;
@@ -714,10 +712,8 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                 p.ws_lse[slot] = row_lse;
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    ptx::mbar_arrive(bars + 8 * kBarOEmpty);
-                    ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1));
-                }
+                ptx::mbar_arrive(bars + 8 * kBarOEmpty, lane == 0);
+                ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1), lane == 0);
                 continue;
             }
             const int qrow = un.q_tile[0] * kBM + row;
@@ -758,10 +754,8 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(bars + 8 * kBarOEmpty);
-                ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1));
-            }
+            ptx::mbar_arrive(bars + 8 * kBarOEmpty, lane == 0);
+            ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1), lane == 0);
             ptx::fence_proxy_async_shared();
             ptx::named_bar_sync(1, 128);
             if (leader) {
@@ -776,12 +770,13 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (un.nkv[t] == 0) continue;
-            if (leader) {
-                const bool ok = ptx::mbar_wait(wc, bars + 8 * (kBarOFull + t), (ph_o >> t) & 1u,
-                                               kSiteEpilogue | (kBarOFull + t)) &&
-                                ptx::mbar_wait(wc, bars + 8 * (kBarStFull + t), (ph_t >> t) & 1u,
-                                               kSiteEpilogue | (kBarStFull + t));
-                go[0] = ok ? 1u : 0u;
+            if (wq == 0) {   // the leader's warp waits, all lanes together
+                const bool ok = __all_sync(0xffffffffu,
+                                           ptx::mbar_wait(wc, bars + 8 * (kBarOFull + t), (ph_o >> t) & 1u,
+                                                          kSiteEpilogue | (kBarOFull + t)) &&
+                                               ptx::mbar_wait(wc, bars + 8 * (kBarStFull + t), (ph_t >> t) & 1u,
+                                                              kSiteEpilogue | (kBarStFull + t)));
+                if (leader) go[0] = ok ? 1u : 0u;
             }
             ptx::named_bar_sync(1, 128);
             if (go[0] == 0u) goto done;
@@ -791,7 +786,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             ptx::tc_fence_after();
             const float4 st = stats[t * kBM + row];
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarStEmpty + t));
+            ptx::mbar_arrive(bars + 8 * (kBarStEmpty + t), lane == 0);
             const float inv_l = 1.0f / st.z;   // the sum of the P values the MMAs used
             const float row_lse = (st.y + ptx::lg2(st.x)) * kLn2;
             if constexpr (kSplit) {
@@ -817,7 +812,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                 p.ws_lse[slot] = row_lse;
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t));
+                ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t), lane == 0);
                 FA_TRACE_EV(leader, kTrEpilogue, kEvEpiDone, t);
                 continue;
             }
@@ -854,7 +849,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                 if (box == C::kBoxes - 1) {
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t));
+                    ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t), lane == 0);
                 }
                 ptx::fence_proxy_async_shared();
                 ptx::named_bar_sync(1, 128);
@@ -878,6 +873,7 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
                                           const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t smem_base,
                                           uint32_t bars)
 {
+    const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
     using C = Cfg<D>;
     uint32_t ph_qe = 0u;       // phase bit of Q buffer t at bit t
     uint32_t q_issued = 0u;    // bit t: a Q load into buffer t was issued
@@ -897,13 +893,13 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
             }
             ph_qe ^= 1u << t;
             const uint32_t fb = bars + 8 * (kBarQFull + t);
-            ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
+            ptx::mbar_arrive_expect_tx(fb, C::kTileBytes, ex);
             const uint32_t dst = smem_base + C::kOffQ + t * C::kTileBytes;
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx)
-                ptx::tma_load_3d(tm_q, dst + bx * C::kBoxBytes, fb, bx * 64, un.q_tile[t] * kBM, un.bh);
+                ptx::tma_load_3d(tm_q, dst + bx * C::kBoxBytes, fb, bx * 64, un.q_tile[t] * kBM, un.bh, ex);
             q_issued |= 1u << t;
-            FA_TRACE_EV(true, kTrLoad, kEvQLoad, t);
+            FA_TRACE_EV(ex != 0u, kTrLoad, kEvQLoad, t);
         }
         for (int j = un.j0; j < un.nmax && ok; ++j) {
 #pragma unroll 1
@@ -921,13 +917,13 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
                 }
                 ++kv_count;
                 const uint32_t fb = bars + 8 * (kBarKVFull + (C::kFullPairs ? (idx / 2u) % C::kPairs : slot));
-                ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
+                ptx::mbar_arrive_expect_tx(fb, C::kTileBytes, ex);
                 const uint32_t dst = smem_base + C::kOffKV + slot * C::kTileBytes;
                 const CUtensorMap* m = kind ? tm_v : tm_k;
 #pragma unroll
                 for (int bx = 0; bx < C::kBoxes; ++bx)
-                    ptx::tma_load_3d(m, dst + bx * C::kBoxBytes, fb, bx * 64, j * kBN, un.bh);
-                FA_TRACE_EV(true, kTrLoad, kEvKVLoad, idx);
+                    ptx::tma_load_3d(m, dst + bx * C::kBoxBytes, fb, bx * 64, j * kBN, un.bh, ex);
+                FA_TRACE_EV(ex != 0u, kTrLoad, kEvKVLoad, idx);
             }
         }
     }
@@ -946,7 +942,7 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
         const uint32_t qmax = (kv_count - 1) / 2;   // the last pair with a copy issued
         // a pair left with only its K copy (an abort in between) gets its
         // second arrival here, so its phase completes once that copy lands
-        if (kv_count & 1u) ptx::mbar_arrive(bars + 8 * (kBarKVFull + qmax % C::kPairs));
+        if (kv_count & 1u) ptx::mbar_arrive(bars + 8 * (kBarKVFull + qmax % C::kPairs), ex);
         for (uint32_t b = 0; b < (uint32_t)C::kPairs && b <= qmax; ++b) {
             const uint32_t q = qmax - ((qmax - b) % C::kPairs);   // last pair on barrier b
             ptx::mbar_wait_drain(wc, bars + 8 * (kBarKVFull + b), (q / C::kPairs) & 1u, kSiteDrain | (kBarKVFull + b));
@@ -1002,7 +998,7 @@ __device__ __forceinline__ void vconvert_role(const Params& p, const ptx::WaitCt
             }
             ptx::fence_proxy_async_shared();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bars + 8 * (C::kBarVConv + iv % C::kSlots));
+            ptx::mbar_arrive(bars + 8 * (C::kBarVConv + iv % C::kSlots), lane == 0);
         }
     }
 }
@@ -1013,6 +1009,7 @@ template <int D, bool kBF16, bool kSplit, bool kDec>
 __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem, uint32_t smem_base,
                                          uint32_t bars)
 {
+    const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);   // Q, K both K-major
     constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, p_is_bf16<kBF16>(), true);   // V MN-major (D contiguous)
@@ -1044,7 +1041,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         }
     };
     // frees the pair of ring entries ending at `idx` (see Cfg): one commit
-    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs)); };
+    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs), ex); };
     // S_t = Q_t K^T: M = 128 rows, N = 128 keys, K = D in steps of 16 (32 bytes
     // inside a 128-byte swizzled row; the next 64 columns sit in the next box).
     // Descriptors are built once per tile and stepped by adding the offset to
@@ -1059,7 +1056,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
             ptx::mma_ss(tmem + C::col_s(t), ptx::sdesc_join(qa + off, kDescHi), ptx::sdesc_join(kb + off, kDescHi),
-                        kIdescQK, kk > 0 ? 1u : 0u);
+                        kIdescQK, kk > 0 ? 1u : 0u, ex);
         }
     };
     // O_t += P_t V: A = P from TMEM (16 keys = 8 columns per step), B = V tile
@@ -1073,7 +1070,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = half * 4 + k4;
             ptx::mma_ts(tmem + C::col_o(t), tmem + C::col_p(t, kDec) + kk * 8,
-                        ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                        ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || kk > 0) ? 1u : 0u, ex);
         }
     };
 
@@ -1083,7 +1080,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         if (un.status == kUnitSkip) continue;
         // K_j is entry kvb + 2(j - j0) of the ring, V_j the entry after it
         const uint32_t kvb = kv_count;
-        FA_TRACE_EV(true, kTrMma, kEvUnit, un.id);
+        FA_TRACE_EV(ex != 0u, kTrMma, kEvUnit, un.id);
         // the unit's first QKs, tile by tile: Q_1 frees only with the previous
         // unit's very last QK and lands last, so QK_0 (and tile 0's softmax)
         // need not wait for it
@@ -1099,9 +1096,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             }
             ptx::tc_fence_after();
             issue_qk(t, kvb);
-            ptx::mma_commit(bars + 8 * (kBarSFull + t));
-            FA_TRACE_EV(true, kTrMma, kEvQK, (uint32_t)t << 12);
-            if (un.nkv[t] == un.j0 + 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
+            ptx::mma_commit(bars + 8 * (kBarSFull + t), ex);
+            FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, (uint32_t)t << 12);
+            if (un.nkv[t] == un.j0 + 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t), ex);
         }
         kv_release(kvb);
         for (int j = un.j0; j < un.nmax; ++j) {
@@ -1110,7 +1107,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (j < un.nkv[t]) {
-                    FA_TRACE_EV(true, kTrMma, kEvPWait, ((uint32_t)t << 12) | j);
+                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPWait, ((uint32_t)t << 12) | j);
                     if (!ptx::mbar_wait(wc, bars + 8 * (kBarPHalf + t), (ph_ph >> t) & 1u, kSiteMma | (kBarPHalf + t)))
                         goto done;
                     ph_ph ^= 1u << t;
@@ -1126,16 +1123,16 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                         v_ready = true;
                     }
                     ptx::tc_fence_after();
-                    FA_TRACE_EV(true, kTrMma, kEvPVGo, ((uint32_t)t << 12) | j);
+                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPVGo, ((uint32_t)t << 12) | j);
                     issue_pv(t, iv, 0, j > un.j0);
-                    FA_TRACE_EV(true, kTrMma, kEvPVMid, ((uint32_t)t << 12) | j);
+                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPVMid, ((uint32_t)t << 12) | j);
                     if (!ptx::mbar_wait(wc, bars + 8 * (kBarPFull + t), (ph_p >> t) & 1u, kSiteMma | (kBarPFull + t)))
                         goto done;
                     ph_p ^= 1u << t;
                     ptx::tc_fence_after();
                     issue_pv(t, iv, 1, true);
-                    FA_TRACE_EV(true, kTrMma, kEvPV, ((uint32_t)t << 12) | j);
-                    if (j == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarOFull + t));
+                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPV, ((uint32_t)t << 12) | j);
+                    if (j == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarOFull + t), ex);
                 }
                 if (j + 1 < un.nkv[t]) {
                     if (!k_ready) {
@@ -1143,11 +1140,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                         k_ready = true;
                         ptx::tc_fence_after();
                     }
-                    FA_TRACE_EV(true, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
+                    FA_TRACE_EV(ex != 0u, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
                     issue_qk(t, ik);
-                    ptx::mma_commit(bars + 8 * (kBarSFull + t));
-                    FA_TRACE_EV(true, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
-                    if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t));
+                    ptx::mma_commit(bars + 8 * (kBarSFull + t), ex);
+                    FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
+                    if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t), ex);
                 }
             }
             // V_j and K_{j+1} together; a unit's last V goes with the next
@@ -1158,7 +1155,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     }
 done:
     // every MMA must be complete before tensor memory is released
-    ptx::mma_commit(bars + 8 * kBarDrain);
+    ptx::mma_commit(bars + 8 * kBarDrain, ex);
     ptx::mbar_wait_drain(wc, bars + 8 * kBarDrain, 0u, kSiteDrain | kBarDrain);
 }
 
@@ -1173,6 +1170,7 @@ template <int D, bool kBF16, bool kSplit>
 __device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem, uint32_t smem_base,
                                             uint32_t bars)
 {
+    const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
     using C = Cfg<D>;
     static_assert(C::kSepP && C::kFullPairs, "key split: D=64 layout");
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);
@@ -1186,7 +1184,7 @@ __device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx&
         const uint32_t q = idx / 2u, b = kBarKVFull + q % C::kPairs;
         return ptx::mbar_wait(wc, bars + 8 * b, (q / C::kPairs) & 1u, kSiteMma | b);
     };
-    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs)); };
+    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs), ex); };
     auto s_free = [&]() -> bool {   // both warpgroups read the previous S
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -1203,7 +1201,7 @@ __device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx&
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
             ptx::mma_ss(tmem + C::col_s(0), ptx::sdesc_join(qa + off, kDescHi), ptx::sdesc_join(kb + off, kDescHi),
-                        kIdescQK, kk > 0 ? 1u : 0u);
+                        kIdescQK, kk > 0 ? 1u : 0u, ex);
         }
     };
     auto issue_pv = [&](int h, uint32_t idx, bool acc) {
@@ -1212,7 +1210,7 @@ __device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx&
         for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = h * 4 + k4;   // key rows 16kk .. 16kk+15 of the tile
             ptx::mma_ts(tmem + C::col_o(h), tmem + C::col_p(0, true) + kk * 8,
-                        ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || k4 > 0) ? 1u : 0u);
+                        ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || k4 > 0) ? 1u : 0u, ex);
         }
     };
     auto v_wait = [&](uint32_t idx) -> bool {   // V_j converted (bf16 inputs)
@@ -1231,16 +1229,16 @@ __device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx&
         if (un.status == kUnitSkip) continue;
         const uint32_t kvb = kv_count;
         const int nkv = un.nkv[0];
-        FA_TRACE_EV(true, kTrMma, kEvUnit, un.id);
+        FA_TRACE_EV(ex != 0u, kTrMma, kEvUnit, un.id);
         if (nkv > un.j0) {
             if (!ptx::mbar_wait(wc, bars + 8 * kBarQFull, ph_q, kSiteMma | kBarQFull)) goto done;
             ph_q ^= 1u;
             if (!s_free() || !kv_wait(kvb)) goto done;
             ptx::tc_fence_after();
             issue_qk(kvb);
-            ptx::mma_commit(bars + 8 * kBarSFull);
-            FA_TRACE_EV(true, kTrMma, kEvQK, un.j0);
-            if (nkv == un.j0 + 1) ptx::mma_commit(bars + 8 * kBarQEmpty);
+            ptx::mma_commit(bars + 8 * kBarSFull, ex);
+            FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, un.j0);
+            if (nkv == un.j0 + 1) ptx::mma_commit(bars + 8 * kBarQEmpty, ex);
         }
         kv_release(kvb);
         for (int j = un.j0; j < un.nmax; ++j) {
@@ -1248,17 +1246,17 @@ __device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx&
             if (j + 1 < nkv) {
                 if (!s_free() || !kv_wait(ik)) goto done;
                 ptx::tc_fence_after();
-                FA_TRACE_EV(true, kTrMma, kEvQKGo, j + 1);
+                FA_TRACE_EV(ex != 0u, kTrMma, kEvQKGo, j + 1);
                 issue_qk(ik);
-                ptx::mma_commit(bars + 8 * kBarSFull);
-                FA_TRACE_EV(true, kTrMma, kEvQK, j + 1);
-                if (j + 1 == nkv - 1) ptx::mma_commit(bars + 8 * kBarQEmpty);
+                ptx::mma_commit(bars + 8 * kBarSFull, ex);
+                FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, j + 1);
+                if (j + 1 == nkv - 1) ptx::mma_commit(bars + 8 * kBarQEmpty, ex);
             }
             if (j < nkv) {
                 if (!v_wait(iv)) goto done;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    FA_TRACE_EV(true, kTrMma, kEvPWait, ((uint32_t)h << 12) | j);
+                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPWait, ((uint32_t)h << 12) | j);
                     if (!ptx::mbar_wait(wc, bars + 8 * (kBarPFull + h), (ph_p >> h) & 1u, kSiteMma | (kBarPFull + h)))
                         goto done;
                     ph_p ^= 1u << h;
@@ -1270,11 +1268,11 @@ __device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx&
                         ph_oe ^= 1u << h;
                     }
                     ptx::tc_fence_after();
-                    FA_TRACE_EV(true, kTrMma, kEvPVGo, ((uint32_t)h << 12) | j);
+                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPVGo, ((uint32_t)h << 12) | j);
                     issue_pv(h, iv, j > un.j0);
-                    FA_TRACE_EV(true, kTrMma, kEvPV, ((uint32_t)h << 12) | j);
-                    ptx::mma_commit(bars + 8 * (kBarPVDone + h));   // P_h, O_h may be rewritten
-                    if (j == nkv - 1) ptx::mma_commit(bars + 8 * (kBarOFull + h));
+                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPV, ((uint32_t)h << 12) | j);
+                    ptx::mma_commit(bars + 8 * (kBarPVDone + h), ex);   // P_h, O_h may be rewritten
+                    if (j == nkv - 1) ptx::mma_commit(bars + 8 * (kBarOFull + h), ex);
                 }
             }
             if (j + 1 < un.nmax) kv_release(ik);
@@ -1282,7 +1280,7 @@ __device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx&
         kv_count = kvb + 2 * (un.nmax - un.j0);
     }
 done:
-    ptx::mma_commit(bars + 8 * kBarDrain);
+    ptx::mma_commit(bars + 8 * kBarDrain, ex);
     ptx::mbar_wait_drain(wc, bars + 8 * kBarDrain, 0u, kSiteDrain | kBarDrain);
 }
 
@@ -1366,13 +1364,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             correction_epilogue_role<D, kBF16, kSplit, kDec>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
     } else {
         ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kControl>();
+        // the loader and the MMA issuer run on all 32 lanes of their warp (one
+        // lane issues), so neither warp diverges while it waits
         if (warp == 12) {
-            if (lane == 0) load_role<D, kSplit>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
+            load_role<D, kSplit>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {
-            if (lane == 0) {
-                if constexpr (kDec) mma_role_ks<D, kBF16, kSplit>(p, wc, tmem, base, bars);
-                else mma_role<D, kBF16, kSplit, kDec>(p, wc, tmem, base, bars);
-            }
+            if constexpr (kDec) mma_role_ks<D, kBF16, kSplit>(p, wc, tmem, base, bars);
+            else mma_role<D, kBF16, kSplit, kDec>(p, wc, tmem, base, bars);
         } else if constexpr (conv_warps<kBF16, kSplit, kDec>() == 6) {
             vconvert_role<D, kSplit, 6>(p, wc, base, bars, 128 + threadIdx.x - 14 * 32);
         } else if constexpr (conv_warps<kBF16, kSplit, kDec>() == 2) {

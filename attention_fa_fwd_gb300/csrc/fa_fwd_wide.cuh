@@ -32,8 +32,9 @@
 // Rescale: the conditional re-base of "G6: Cluster 与 2CTA 探索", V41 (base b
 // moves only when the row maximum passes b + T; T = 15 for fp16, 30 for bf16,
 // as in the two-tile kernel), warp-wide as there; the softmax warps rescale O
-// in TMEM themselves ("G6", V44), each warpgroup its half of O's columns;
-// only then do they wait for the previous P*V to complete.  bf16 rows
+// in TMEM themselves ("G6", V44), each warpgroup its half of O's columns,
+// after the previous P*V has completed; the first P*V half of the step writes
+// every column of O, so it waits for warpgroup 1 too (see kBarPA).  bf16 rows
 // normalise O by l + dl, dl adding per step the rounding of each half's
 // largest p to bf16 (as the two-tile kernel does).  This layout keeps P in
 // bf16 for bf16 inputs (no conversion of V).
@@ -93,10 +94,13 @@ struct WideCfg {
         kBarSFull = 4,      // scores of the step in TMEM (commit)
         kBarSFree = 5,      // both softmax warpgroups read S (8 warps)
         // [2] per P buffer: P of keys [0, BN/2) (PA) or [BN/2, BN) (PB) in
-        // TMEM, O rescaled (4 warps each).  One barrier per buffer, not one
-        // per role: the softmax may publish the next step's P before the
-        // issuer has waited on this step's, and a single barrier would then
-        // complete two phases and read as incomplete.
+        // TMEM, O rescaled.  PB: warpgroup 1's 4 warps.  PA: warpgroup 0's 4
+        // warps and warpgroup 1's 4: the first P*V half writes every column
+        // of O, so it must also wait until warpgroup 1 has left O alone (its
+        // half of O's columns rescaled, when the step rescales).  One barrier
+        // per buffer, not one per role: the softmax may publish the next
+        // step's P before the issuer has waited on this step's, and a single
+        // barrier would then complete two phases and read as incomplete.
         kBarPA = 6,
         kBarPB = 8,
         kBarPVDone = 10,    // the step's P*V finished: O may be rescaled (commit)
@@ -253,7 +257,7 @@ __device__ __forceinline__ void wide_softmax_role(const Params& p, const ptx::Wa
             // S is in registers: the issuer may compute the next step's scores
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bars + 8 * C::kBarSFree);
+            ptx::mbar_arrive(bars + 8 * C::kBarSFree, lane == 0);
             WT_MARK(0);
             float* s = reinterpret_cast<float*>(sr);
             const int k0 = j * C::kBN + w * NC;   // first key of this half
@@ -296,6 +300,9 @@ __device__ __forceinline__ void wide_softmax_role(const Params& p, const ptx::Wa
                 h = ptx::ex2(b - cand);   // 0 on the first step (b = -inf); 1 if cand == b
                 b = cand;
             }
+            // warpgroup 1 without a rescale this step leaves O alone: the first
+            // P*V half (warpgroup 0's keys, every column of O) need not wait for it
+            if (w == 1 && !rescale) ptx::mbar_arrive(bars + 8 * (C::kBarPA + (st & 1u)), lane == 0);
             // p = 2^(s * scale*log2e - b), packed to 16 bits two keys a word and
             // stored 32 keys at a time into this step's P buffer
             const float nb = (b == -INFINITY) ? 0.f : -b;
@@ -339,7 +346,9 @@ __device__ __forceinline__ void wide_softmax_role(const Params& p, const ptx::Wa
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar_p + 8 * (st & 1u));
+            ptx::mbar_arrive(bar_p + 8 * (st & 1u), lane == 0);
+            // warpgroup 1's rescaled half of O, for the first P*V half
+            if (w == 1 && rescale) ptx::mbar_arrive(bars + 8 * (C::kBarPA + (st & 1u)), lane == 0);
             WT_MARK(3);
             WT_STEP();
             float sa, sb;
@@ -352,7 +361,7 @@ __device__ __forceinline__ void wide_softmax_role(const Params& p, const ptx::Wa
             return;
         stats[(ob * 2 + w) * kBM + row] = make_float4(l, l + dl, b, 0.f);
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars + 8 * (C::kBarStFull + ob));
+        ptx::mbar_arrive(bars + 8 * (C::kBarStFull + ob), lane == 0);
         ++cnt;
     }
     WT_FLUSH(w);
@@ -384,7 +393,7 @@ __device__ __forceinline__ void wide_epilogue_role(const Params& p, const ptx::W
         const float4 s0 = stats[(ob * 2 + 0) * kBM + row];
         const float4 s1 = stats[(ob * 2 + 1) * kBM + row];
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars + 8 * (C::kBarStEmpty + ob));
+        ptx::mbar_arrive(bars + 8 * (C::kBarStEmpty + ob), lane == 0);
         const float inv = 1.0f / (s0.y + s1.y);
         const int qrow = un.q_tile * kBM + row;
         const bool in = qrow < p.S;
@@ -400,7 +409,7 @@ __device__ __forceinline__ void wide_epilogue_role(const Params& p, const ptx::W
                 // every column read: the issuer may start the next unit's P*V here
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bars + 8 * (C::kBarOEmpty + ob));
+                ptx::mbar_arrive(bars + 8 * (C::kBarOEmpty + ob), lane == 0);
             }
             uint32_t pk[16];
 #pragma unroll
@@ -657,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bars + 8 * C::kBarSFull, 1);
         ptx::mbar_init(bars + 8 * C::kBarSFree, 8);
         for (int t = 0; t < 2; ++t) {
-            ptx::mbar_init(bars + 8 * (C::kBarPA + t), 4);
+            ptx::mbar_init(bars + 8 * (C::kBarPA + t), 8);
             ptx::mbar_init(bars + 8 * (C::kBarPB + t), 4);
         }
         ptx::mbar_init(bars + 8 * C::kBarPVDone, 1);

@@ -65,6 +65,18 @@ def test_head_dim_64_one_tile_per_unit(dtype, causal):
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_64_key_split_edges(dtype, causal):
+    # one tile per unit at D=64: the two warpgroups take keys 0-63 and 64-127
+    # of every key tile and the epilogue merges them; sequence ends on, just
+    # before and just after a half boundary, so one half is empty in the last
+    # tile (or, causal, in the first rows' only tile)
+    for S in (63, 64, 65, 191, 192, 193):
+        assert _tiles_per_unit(1, 2, S, 64, causal) == 1
+        check_full(1, 2, S, 64, dtype, causal, seed=S)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("D,scale", [(64, 2.0), (128, 2.0), (64, 1e-3), (128, 1e-3)])
 def test_extreme_scales(D, scale, causal, dtype):
     """scale 2: scores of std 2*sqrt(D), rows close to one-hot, and the running
