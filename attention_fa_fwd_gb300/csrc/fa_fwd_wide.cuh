@@ -284,7 +284,7 @@ __device__ __forceinline__ void wide_softmax_role(const Params& p, const ptx::Wa
             float* xs = xchg + (st & 1u) * (2 * kBM);
             xs[w * kBM + row] = mraw;
             __syncwarp();
-            if (lane == 0) ptx::st_release_shared(flag_own, st + 1u);
+            ptx::st_release_shared(flag_own, st + 1u, lane == 0);
             WT_MARK(5);
             if (!ptx::flag_wait_warp(wc, flag_partner, st + 1u, kSiteSoftmax | 0xF0u)) return;
             WT_MARK(6);
@@ -438,6 +438,7 @@ __device__ __forceinline__ void wide_load_role(const Params& p, const ptx::WaitC
                                                const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t smem_base,
                                                uint32_t bars)
 {
+    const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
     using C = WideCfg<D>;
     uint32_t e = 0;        // ring entries issued
     uint32_t nq = 0;       // Q tiles issued
@@ -449,11 +450,11 @@ __device__ __forceinline__ void wide_load_role(const Params& p, const ptx::WaitC
             return;
         }
         const uint32_t fb = bars + 8 * (C::kBarQFull + qb);
-        ptx::mbar_arrive_expect_tx(fb, C::kQBytes);
+        ptx::mbar_arrive_expect_tx(fb, C::kQBytes, ex);
         const uint32_t dst = smem_base + C::kOffQ + qb * C::kQBytes;
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
-            ptx::tma_load_3d(tm_q, dst + bx * C::kQBoxBytes, fb, bx * 64, u.q_tile * kBM, u.bh);
+            ptx::tma_load_3d(tm_q, dst + bx * C::kQBoxBytes, fb, bx * 64, u.q_tile * kBM, u.bh, ex);
         ++nq;
     };
     auto load_kv = [&](const CUtensorMap* m, const WideUnit& u, int j) {
@@ -464,11 +465,11 @@ __device__ __forceinline__ void wide_load_role(const Params& p, const ptx::WaitC
             return;
         }
         const uint32_t fb = bars + 8 * (C::kBarKVFull + slot);
-        ptx::mbar_arrive_expect_tx(fb, C::kKVBytes);
+        ptx::mbar_arrive_expect_tx(fb, C::kKVBytes, ex);
         const uint32_t dst = smem_base + C::kOffKV + slot * C::kKVBytes;
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
-            ptx::tma_load_3d(m, dst + bx * C::kKVBoxBytes, fb, bx * 64, j * C::kBN, u.bh);
+            ptx::tma_load_3d(m, dst + bx * C::kKVBoxBytes, fb, bx * 64, j * C::kBN, u.bh, ex);
         ++e;
     };
 
@@ -517,6 +518,7 @@ template <int D, bool kBF16>
 __device__ __forceinline__ void wide_mma_role(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem,
                                               uint32_t smem_base, uint32_t bars)
 {
+    const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
     using C = WideCfg<D>;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, C::kBN, kBF16, false);   // Q, K both K-major
     constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, kBF16, true);         // V is MN-major (D contiguous)
@@ -532,7 +534,7 @@ __device__ __forceinline__ void wide_mma_role(const Params& p, const ptx::WaitCt
             const uint32_t oa = ((kk >> 2) * C::kQBoxBytes + (kk & 3) * 32) >> 4;
             const uint32_t ob = ((kk >> 2) * C::kKVBoxBytes + (kk & 3) * 32) >> 4;
             ptx::mma_ss(tmem + C::kColS, ptx::sdesc_join(qa + oa, kDescHi), ptx::sdesc_join(kb + ob, kDescHi),
-                        kIdescQK, kk > 0 ? 1u : 0u);
+                        kIdescQK, kk > 0 ? 1u : 0u, ex);
         }
     };
     // O += P V for one half of the keys: A = P from TMEM (16 keys = 8 columns
@@ -543,7 +545,7 @@ __device__ __forceinline__ void wide_mma_role(const Params& p, const ptx::WaitCt
         for (int k4 = 0; k4 < kHalfK; ++k4) {
             const int kk = half * kHalfK + k4;
             ptx::mma_ts(tmem + C::kColO + ob * D, tmem + C::kColP + pb * (C::kBN / 2) + kk * 8,
-                        ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                        ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || kk > 0) ? 1u : 0u, ex);
         }
     };
     auto kv_wait = [&](uint32_t e) {
@@ -555,7 +557,7 @@ __device__ __forceinline__ void wide_mma_role(const Params& p, const ptx::WaitCt
     uint32_t e = 0;     // ring entries consumed (same order as the loader's)
     uint32_t st = 0;    // steps
     uint32_t cnt = 0;   // units
-    WT_DECL(true);
+    WT_DECL(ex != 0u);
     int r = -1;
     WideUnit un = wide_next_unit<C::kBN>(r, p);
     if (un.status == kUnitOk) {
@@ -563,9 +565,9 @@ __device__ __forceinline__ void wide_mma_role(const Params& p, const ptx::WaitCt
         if (!ptx::mbar_wait(wc, bars + 8 * C::kBarQFull, 0u, kSiteMma | C::kBarQFull) || !kv_wait(0)) goto done;
         ptx::tc_fence_after();
         issue_qk(0, 0);
-        ptx::mma_commit(bars + 8 * C::kBarSFull);
-        ptx::mma_commit(bars + 8 * C::kBarKVEmpty);
-        if (un.n == 1) ptx::mma_commit(bars + 8 * C::kBarQEmpty);
+        ptx::mma_commit(bars + 8 * C::kBarSFull, ex);
+        ptx::mma_commit(bars + 8 * C::kBarKVEmpty, ex);
+        if (un.n == 1) ptx::mma_commit(bars + 8 * C::kBarQEmpty, ex);
         e = 1;
     }
     while (un.status == kUnitOk) {
@@ -596,9 +598,9 @@ __device__ __forceinline__ void wide_mma_role(const Params& p, const ptx::WaitCt
                 WT_MARK(2);
                 ptx::tc_fence_after();
                 issue_qk(nqb, ek % C::kSlots);
-                ptx::mma_commit(bars + 8 * C::kBarSFull);
-                ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + ek % C::kSlots));
-                if (nj == nn - 1) ptx::mma_commit(bars + 8 * (C::kBarQEmpty + nqb));
+                ptx::mma_commit(bars + 8 * C::kBarSFull, ex);
+                ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + ek % C::kSlots), ex);
+                if (nj == nn - 1) ptx::mma_commit(bars + 8 * (C::kBarQEmpty + nqb), ex);
                 WT_MARK(3);
             }
             // P*V of this step
@@ -617,9 +619,9 @@ __device__ __forceinline__ void wide_mma_role(const Params& p, const ptx::WaitCt
             WT_MARK(6);
             ptx::tc_fence_after();
             issue_pv(ev % C::kSlots, ob, pb, 1, true);
-            ptx::mma_commit(bars + 8 * C::kBarPVDone);
-            ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + ev % C::kSlots));
-            if (j == un.n - 1) ptx::mma_commit(bars + 8 * (C::kBarOFull + ob));
+            ptx::mma_commit(bars + 8 * C::kBarPVDone, ex);
+            ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + ev % C::kSlots), ex);
+            if (j == un.n - 1) ptx::mma_commit(bars + 8 * (C::kBarOFull + ob), ex);
             WT_MARK(7);
             WT_STEP();
         }
@@ -629,7 +631,7 @@ __device__ __forceinline__ void wide_mma_role(const Params& p, const ptx::WaitCt
     }
 done:
     // every MMA must be complete before tensor memory is released
-    ptx::mma_commit(bars + 8 * C::kBarDrain);
+    ptx::mma_commit(bars + 8 * C::kBarDrain, ex);
     ptx::mbar_wait_drain(wc, bars + 8 * C::kBarDrain, 0u, kSiteDrain | C::kBarDrain);
     WT_FLUSH(kTrMma);
 }
@@ -704,10 +706,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         wide_epilogue_role<D, kBF16>(p, wc, tmem, bars, stats);
     } else {
         ptx::setmaxnreg_dec<WideRegs::kControl>();
+        // the loader and the MMA issuer run on all 32 lanes of their warp (one
+        // lane issues), so neither warp diverges while it waits
         if (warp == 12) {
-            if (lane == 0) wide_load_role<D>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
+            wide_load_role<D>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {
-            if (lane == 0) wide_mma_role<D, kBF16>(p, wc, tmem, base, bars);
+            wide_mma_role<D, kBF16>(p, wc, tmem, base, bars);
         }
         __syncwarp();
     }

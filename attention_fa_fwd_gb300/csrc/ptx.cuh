@@ -152,9 +152,12 @@ __device__ __forceinline__ bool mbar_wait_drain(const WaitCtx& w, uint32_t bar, 
 
 // Shared-memory word with release / acquire semantics at CTA scope: a step
 // counter one warp publishes after its data, another polls before reading it.
-__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v)
+__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v, uint32_t on = 1u)
 {
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q st.release.cta.shared::cta.u32 [%0], %1;\n\t}" ::"r"(addr), "r"(v), "r"(on)
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr)
