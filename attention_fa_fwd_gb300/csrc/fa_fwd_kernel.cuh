@@ -134,9 +134,6 @@ constexpr float kLn2 = 0.693147180559945309f;
 // splits are the spill-free ones ptxas -v reports for each head dim and type
 //
 template <int D, bool kBF16, bool kSplit, bool kDec> struct RegSplit {   // D=128 one pass, D=64 split-KV
-    static constexpr uint32_t kSoftmax = 184, kEpilogue = 64, kControl = 80;
-};
-template <bool kBF16> struct RegSplit<128, kBF16, true, false> {
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 56, kControl = 88;
 };
 template <bool kBF16, bool kDec> struct RegSplit<64, kBF16, false, kDec> {
@@ -145,7 +142,7 @@ template <bool kBF16, bool kDec> struct RegSplit<64, kBF16, false, kDec> {
 // key split (decoupled instances): a warpgroup holds 64 scores per row, and the
 // epilogue merges two accumulators
 template <bool kBF16> struct RegSplit<64, kBF16, false, true> {
-    static constexpr uint32_t kSoftmax = 168, kEpilogue = 104, kControl = 72;
+    static constexpr uint32_t kSoftmax = 160, kEpilogue = 120, kControl = 72;
 };
 template <bool kBF16> struct RegSplit<64, kBF16, true, true> {
     static constexpr uint32_t kSoftmax = 168, kEpilogue = 104, kControl = 72;
@@ -1299,7 +1296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bars = base + C::kOffBars;
     float4* stats = reinterpret_cast<float4*>(smem + C::kOffStats);
     volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(smem + C::kOffCtl);
-    const int warp = threadIdx.x >> 5;
+    const int warp = ptx::warp_id_uniform();
     const int lane = threadIdx.x & 31;
     FA_TRACE_DECL;
     FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvEntry, 0);

@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xchg = reinterpret_cast<float*>(smem + C::kOffX);
     float4* stats = reinterpret_cast<float4*>(smem + C::kOffSt);
     volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(smem + C::kOffCtl);
-    const int warp = threadIdx.x >> 5;
+    const int warp = ptx::warp_id_uniform();
     const int lane = threadIdx.x & 31;
     // the next kernel in the stream may be scheduled now (see the two-tile kernel)
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -20,6 +20,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The warp's index in the block, broadcast from lane 0 so the compiler can
+// prove it warp-uniform: code under branches on it then stays on the uniform
+// datapath (tcgen05 takes its descriptors and tensor-memory addresses from
+// uniform registers).  Measured 4-9% over threadIdx.x / 32 at the kernel's
+// role dispatch (inside the roles the warp's quarter stays threadIdx.x-based:
+// broadcasting it too measured 1-2% slower on the large workloads).
+__device__ __forceinline__ int warp_id_uniform()
+{
+    return __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;
