@@ -139,13 +139,12 @@ template <int D, bool kBF16, bool kSplit, bool kDec> struct RegSplit {   // D=12
 template <bool kBF16, bool kDec> struct RegSplit<64, kBF16, false, kDec> {
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72;
 };
-// key split (decoupled instances): a warpgroup holds 64 scores per row, and the
-// epilogue merges two accumulators
+// key-parity units (kDec): the epilogue merges two accumulators
 template <bool kBF16> struct RegSplit<64, kBF16, false, true> {
-    static constexpr uint32_t kSoftmax = 160, kEpilogue = 120, kControl = 72;
+    static constexpr uint32_t kSoftmax = 176, kEpilogue = 88, kControl = 72;
 };
 template <bool kBF16> struct RegSplit<64, kBF16, true, true> {
-    static constexpr uint32_t kSoftmax = 168, kEpilogue = 104, kControl = 72;
+    static constexpr uint32_t kSoftmax = 176, kEpilogue = 88, kControl = 72;
 };
 template <int D, bool kBF16, bool kSplit, bool kDec>
 constexpr bool reg_split_fits()
@@ -170,21 +169,24 @@ enum : int {
     kBarStFull = 14,    // [2] row statistics of tile t in shared memory (4 softmax warps)
     kBarStEmpty = 16,   // [2] epilogue took the statistics (4 epilogue warps)
     kBarDrain = 18,     // MMA drain at exit (commit)
-    kBarSFree = 19,     // [2] separate-P layout: S_t read into registers (4 softmax warps)
-    kBarPVDone = 21,    // [2] separate-P layout: PV_t finished reading P_t (commit)
-    kBarKVFull = 23,    // [slots] K or V tile landed (TMA tx)
+    kBarKVFull = 19,    // [slots] K or V tile landed (TMA tx)
 };
 
-template <int D>
+template <int D, bool kKP = false>
 struct Cfg {
     static_assert(D == 64 || D == 128, "head dim");
+    static_assert(!kKP || D == 64, "key-parity units: head dim 64");
     static constexpr int kTileBytes = kBM * D * 2;          // one Q, K or V tile (16-bit)
     static constexpr int kBoxBytes = kBM * 64 * 2;          // one 128-row x 64-column swizzle box
     static constexpr int kBoxes = D / 64;
-    static constexpr int kSlots = (D == 128) ? 4 : 8;        // K/V ring (K and V share it)
+    // Key-parity units (kKP, one query tile per unit at D=64): a ring entry
+    // holds two key tiles, 2j and 2j+1 of step j (the even one for tile slot 0,
+    // the odd one for slot 1), so the ring keeps its 128 KB in 4 double slots.
+    static constexpr int kSlotBytes = kKP ? 2 * kTileBytes : kTileBytes;
+    static constexpr int kSlots = kKP ? 4 : ((D == 128) ? 4 : 8);   // K/V ring (K and V share it)
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
-    static constexpr int kOffStage = kOffKV + kSlots * kTileBytes;   // one O box for the TMA store
+    static constexpr int kOffStage = kOffKV + kSlots * kSlotBytes;   // one O box for the TMA store
     static constexpr int kOffStats = kOffStage + kBoxBytes;          // float4 (l, b, l_norm, 0) [2][128]
     // Ring entries free in pairs: V_j with the next K_{j+1} (they free
     // together), a unit's last V with the next unit's first K, entry 0 alone;
@@ -208,30 +210,23 @@ struct Cfg {
     static constexpr int kOffBars = kOffStats + 2 * kBM * 16;
     static constexpr int kOffCtl = kOffBars + kNumBars * 8;          // [0] TMEM base, [1] abort, [2] epilogue go
     static constexpr int kSmemBytes = kOffCtl + 16 + 1024;            // + slack to align the base to 1 KB
-    // TMEM columns of the score region S_t, the output accumulator O_t and P_t.
-    // D=128 fills the 512 columns with S0 | S1 | O0 | O1, so P_t overwrites the
-    // first half of S_t and the next QK_t must wait for PV_t.  D=64 leaves 128
-    // columns free.  The decoupled instances (kDec, launched for one query tile
-    // per unit) use S0 for the tile's scores, columns 384-447 for its P and
-    // O0 | O1 for two accumulators: warpgroup h takes keys 64h..64h+63 of every
-    // key tile (scores S0[64h..], P at 384 + 32h, accumulator O_h), so QK(j+1)
-    // can run as soon as both warpgroups have read S(j), while P_h(j) waits for
-    // its PV.  With two tiles per unit P_t stays on S_t: the tiles alternate
-    // anyway, and a decoupled order measured 4-6% slower there (10x64x1024x64).
-    static constexpr bool kSepP = (D == 64);
+    // TMEM columns: S0 | S1 | O0 | O1.  P_t overwrites the first half of S_t,
+    // so the next QK_t must wait for PV_t (the issuer orders them).  In
+    // key-parity units the two slots hold one query tile's even and odd key
+    // tiles: O0 and O1 are two partial accumulators the epilogue merges.
     __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
     __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
-    __device__ static constexpr uint32_t col_p(int t, bool decoupled)
-    {
-        return (kSepP && decoupled) ? 384u + (t ? 64u : 0u) : col_s(t);
-    }
+    __device__ static constexpr uint32_t col_p(int t) { return col_s(t); }
 };
+
+static_assert(Cfg<64, true>::kSmemBytes <= Cfg<64>::kSmemBytes, "key-parity instances fit the D=64 launch geometry");
 
 struct Unit {
     int status;      // kUnitDone, kUnitOk or kUnitSkip
     int id;          // position of the unit in the schedule (split: its workspace slot)
     int bh;
-    int j0;          // first key tile of the unit (0 unless split)
+    int j0;          // first key step of the unit (0 unless split)
+    int kt0;         // key-parity units: first key tile (step j of slot t is key tile kt0 + 2j + t)
     int q_tile[2];   // query tile index of each tile of the unit
     int nkv[2];      // end (exclusive) of the key tiles tile t visits; 0 = tile absent
     int last[2];     // the tile's last key tile overall: the one the mask applies to
@@ -264,7 +259,7 @@ enum : int { kUnitDone = 0, kUnitOk = 1, kUnitSkip = 2 };
 // Returned by value: a unit the caller keeps by reference becomes
 // address-taken and its fields are reloaded from local memory in the MMA
 // issuer's inner loop (measured: 8% slower).
-template <bool kSplit>
+template <bool kSplit, bool kKP = false>
 __device__ __forceinline__ Unit unit_at(int r, const Params& p)
 {
     const long long G = gridDim.x, c = blockIdx.x;
@@ -324,6 +319,25 @@ __device__ __forceinline__ Unit unit_at(int r, const Params& p)
     }
     un.bh = bh;
     un.nmax = 0;
+    un.kt0 = 0;
+    if constexpr (kKP) {
+        // key-parity unit: one query tile (p.tpu == 1); its key tiles
+        // [kt0, end) alternate between slot 0 (even steps of the unit's own
+        // count) and slot 1, step j holding tiles kt0 + 2j and kt0 + 2j + 1
+        const int qt = qg;
+        const int total = kv_tiles_of(qt, p.n_kv, p.causal);
+        const int kt0 = un.j0;
+        const int end = kSplit ? min(kt0 + p.split_chunk, total) : total;
+        const int count = end > kt0 ? end - kt0 : 0;
+        un.kt0 = kt0;
+        un.j0 = 0;
+        un.q_tile[0] = un.q_tile[1] = qt;
+        un.last[0] = un.last[1] = total - 1;
+        un.nkv[0] = (count + 1) / 2;
+        un.nkv[1] = count / 2;
+        un.nmax = un.nkv[0];
+        return un;
+    }
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         const int qt = qg * p.tpu + t;
@@ -377,42 +391,31 @@ template <int D, bool kBF16, bool kSplit, bool kDec>
 __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx& wc, int t, uint32_t tmem,
                                              uint32_t bars, float4* stats)
 {
-    using C = Cfg<D>;
+    // kDec: key-parity units (one query tile; slot t takes its key tiles
+    // kt0 + 2j + t, with its own base, sum and accumulator O_t, merged by the
+    // epilogue).  Otherwise slot t is query tile t of the unit.
+    using C = Cfg<D, kDec>;
     const int lane = threadIdx.x & 31;
     const int wq = (threadIdx.x >> 5) & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_base + (kDec ? C::col_s(0) + 64u * t : C::col_s(t));
+    const uint32_t tS = tmem + lane_base + C::col_s(t);
     const uint32_t tO = tmem + lane_base + C::col_o(t);
-    // decoupled order (separate P): the next QK_t runs before PV_t, so P_t and
-    // O_t wait for that PV explicitly; in the shared order S_t(j) implies that
-    // PV_t(j-1) has finished
-    static_assert(!kDec || C::kSepP, "the decoupled order needs P in its own columns");
-    // Decoupled instances run one query tile per unit and split each key tile
-    // between the two warpgroups (keys 0-63 and 64-127 of every step): each
-    // keeps its own base, row sum and O accumulator (O_t), and the epilogue
-    // merges the two halves.  So a key step's softmax work per warpgroup halves
-    // and no row maximum is exchanged.
-    constexpr bool kKS = kDec;
-    constexpr int kCols = kKS ? 64 : 128;      // S columns this warpgroup reads per key step
-    constexpr int kChunks = kCols / 32;
-    const uint32_t tP = tmem + lane_base + (kKS ? C::col_p(0, true) + 32u * t : C::col_p(t, kDec));
+    const uint32_t tP = tmem + lane_base + C::col_p(t);
     const float sl2 = p.scale_log2;
     uint32_t ph_s = 0, ph_te = 0, ph_o = 0;
-    uint32_t n_pub = 0;   // separate P: P tiles this warpgroup published (one PV each)
     FA_TRACE_DECL;
     const bool tr = (threadIdx.x & 127) == 0;
 
     for (int r = 0;; ++r) {
-        const Unit un = unit_at<kSplit>(r, p);
+        const Unit un = unit_at<kSplit, kDec>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         // t is a runtime value: select instead of indexing, so the unit stays in registers
-        const int tt = kKS ? 0 : t;   // the query tile this warpgroup works on
-        const int nkv = tt ? un.nkv[1] : un.nkv[0];
-        const int q_tile = tt ? un.q_tile[1] : un.q_tile[0];
+        const int nkv = t ? un.nkv[1] : un.nkv[0];
+        const int q_tile = t ? un.q_tile[1] : un.q_tile[0];
         // the masked tile: the row's last key tile (always nkv - 1 without a split)
-        const int last = kSplit ? (tt ? un.last[1] : un.last[0]) : nkv - 1;
+        const int last = (kSplit || kDec) ? (t ? un.last[1] : un.last[0]) : nkv - 1;
         if (nkv == 0) continue;
         float b = -INFINITY;   // base of the row, base-2 scaled units
         float l = 0.f;         // running sum of 2^(x - b): gives the LSE
@@ -425,52 +428,43 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
         // 1.1e-3 off).  fp16 inputs round O to 2^-11 relative: dl stays 0.
         float dl = 0.f;
         for (int j = un.j0; j < nkv; ++j) {
-            // (key split: both warpgroups read the one tile's scores, committed on SFull_0)
-            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + tt), ph_s, kSiteSoftmax | (kBarSFull + tt))) return;
+            const int kt = kDec ? un.kt0 + 2 * j + t : j;   // the key tile in S_t
+            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + t), ph_s, kSiteSoftmax | (kBarSFull + t))) return;
             ph_s ^= 1u;
             FA_TRACE_EV(tr, t, kEvSReady, j);
             ptx::tc_fence_after();
             // scores of the row; each 32-column load also returns its maximum
-            uint32_t sr[kCols];
-            float pm[kChunks];
+            uint32_t sr[128];
+            float pm[4];
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) ptx::tmem_ld32_max(tS + 32 * c, sr + 32 * c, pm[c]);
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32_max(tS + 32 * c, sr + 32 * c, pm[c]);
             ptx::tmem_wait_ld();
             ptx::reg_fence(sr);
             ptx::reg_fence(pm);
-            if constexpr (kDec) {
-                // S is in registers: once both warpgroups are here the MMA issuer may compute the next S
-                ptx::tc_fence_before();
-                __syncwarp();
-                ptx::mbar_arrive(bars + 8 * (kBarSFree + t), lane == 0);
-            }
             FA_TRACE_EV(tr, t, kEvSLoaded, j);
             float* s = reinterpret_cast<float*>(sr);
             float mraw;
-            if (p.mask_last && j == last) {
+            if (p.mask_last && kt == last) {
                 // keys beyond the sequence, and (causal) keys after this row
                 const int qrow = q_tile * kBM + row;
-                int lim = p.S - 1 - j * kBN;
-                if (p.causal) lim = min(lim, qrow - j * kBN);
-                if (kKS) lim -= 64 * t;   // this warpgroup's first key of the tile
+                int lim = p.S - 1 - kt * kBN;
+                if (p.causal) lim = min(lim, qrow - kt * kBN);
 #pragma unroll
-                for (int c = 0; c < kCols; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
-                // maximum over what is left: one chain of three-input max per 32 columns
-                float m[kChunks];
+                for (int c = 0; c < 128; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+                // maximum over what is left: four chains of three-input max
+                float m[4];
 #pragma unroll
-                for (int k = 0; k < kChunks; ++k) m[k] = ptx::max3(s[32 * k], s[32 * k + 1], s[32 * k + 2]);
+                for (int k = 0; k < 4; ++k) m[k] = ptx::max3(s[32 * k], s[32 * k + 1], s[32 * k + 2]);
 #pragma unroll
                 for (int i = 3; i < 31; i += 2) {
 #pragma unroll
-                    for (int k = 0; k < kChunks; ++k) m[k] = ptx::max3(m[k], s[32 * k + i], s[32 * k + i + 1]);
+                    for (int k = 0; k < 4; ++k) m[k] = ptx::max3(m[k], s[32 * k + i], s[32 * k + i + 1]);
                 }
 #pragma unroll
-                for (int k = 0; k < kChunks; ++k) m[k] = fmaxf(m[k], s[32 * k + 31]);
-                if constexpr (kKS) mraw = fmaxf(m[0], m[1]);
-                else mraw = fmaxf(ptx::max3(m[0], m[1], m[2]), m[3]);
+                for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], s[32 * k + 31]);
+                mraw = fmaxf(ptx::max3(m[0], m[1], m[2]), m[3]);
             } else {
-                if constexpr (kKS) mraw = fmaxf(pm[0], pm[1]);
-                else mraw = fmaxf(ptx::max3(pm[0], pm[1], pm[2]), pm[3]);
+                mraw = fmaxf(ptx::max3(pm[0], pm[1], pm[2]), pm[3]);
             }
             const float mx = mraw * sl2;
             // conditional re-base: keep b unless the maximum passed b + T.  The O
@@ -502,15 +496,6 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 b = nb_new;
             }
             FA_TRACE_EV(tr, t, kEvMaxDone, j);
-            if constexpr (kDec) {
-                // P_t and O_t are free once the PV of the previously published P_t
-                // completed (in this order S(j) does not imply it)
-                if (n_pub > 0 && !ptx::mbar_wait_warp(wc, bars + 8 * (kBarPVDone + t), (n_pub - 1) & 1u,
-                                                      kSiteSoftmax | (kBarPVDone + t)))
-                    return;
-                ++n_pub;
-                ptx::tc_fence_after();
-            }
             if (rescale) {
                 // this warp's 32 rows of O_t are scaled by 2^(b_old - b_new)
 #pragma unroll 1
@@ -535,7 +520,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 dl = fmaf(dl, h, ptx::round16<p_is_bf16<kBF16>()>(pm) - pm);
             }
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -553,12 +538,11 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 }
                 ptx::tmem_st16(tP + c * 16, pk);
                 if (c == 1 || c == 3) {
-                    // publish P (and, at c == 1, the rescaled O) for the MMA issuer;
-                    // a key-split warpgroup publishes its 64 keys once, on PFull
+                    // publish P (and, at c == 1, the rescaled O) for the MMA issuer
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
-                    ptx::mbar_arrive(bars + 8 * ((c == 1 && !kKS) ? kBarPHalf + t : kBarPFull + t), lane == 0);
+                    ptx::mbar_arrive(bars + 8 * (c == 1 ? kBarPHalf + t : kBarPFull + t), lane == 0);
                     if (c == 1) FA_TRACE_EV(tr, t, kEvExpDone, j);
                 }
             }
@@ -568,7 +552,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             l = fmaf(l, h, sa + sb);
         }
 #ifdef FA_DEBUG_STATS
-        if (!kSplit && !kKS && p.dbg_rows != nullptr) {
+        if (!kSplit && !kDec && p.dbg_rows != nullptr) {
             // the debug build writes each row's final base and row sum
             const int qrow = q_tile * kBM + row;
             if (qrow < p.S) {
@@ -633,7 +617,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                                                          const CUtensorMap* tm_o, uint32_t tmem, uint32_t smem_base,
                                                          uint32_t bars, const float4* stats, volatile uint32_t* ctl_go)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, kDec>;
     const int lane = threadIdx.x & 31;
     const int wq = (threadIdx.x >> 5) & 3;
     const int row = wq * 32 + lane;
@@ -646,61 +630,70 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
     if constexpr (epi_in_softmax<kBF16, kSplit, kDec>()) return;   // the softmax warpgroups run the epilogue
 
     for (int r = 0;; ++r) {
-        const Unit un = unit_at<kSplit>(r, p);
+        const Unit un = unit_at<kSplit, kDec>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         if constexpr (kDec) {
-            // key split: the unit's one query tile has two partial results, keys
-            // 0-63 (O_0, base b0, sum l0) and 64-127 (O_1, b1, l1) of every key
-            // tile; with m = max(b0, b1) and w_h = 2^(b_h - m) the row's sum is
+            // key-parity unit: the unit's one query tile has two partial
+            // results, slot 0 (its even key tiles: O_0, base b0, sum l0) and
+            // slot 1 (odd: O_1, b1, l1; absent when the unit has one key tile);
+            // with m = max(b0, b1) and w_h = 2^(b_h - m) the row's sum is
             // w0 l0 + w1 l1 and its O is (w0 O_0 + w1 O_1) / (w0 l0' + w1 l1')
             // (l' the normaliser, l + dl)
             if (un.nkv[0] == 0) continue;
+            const bool has1 = un.nkv[1] > 0;
             if (wq == 0) {   // the leader's warp waits, all lanes together
-                bool ok = true;
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
+                bool ok = ptx::mbar_wait(wc, bars + 8 * kBarOFull, ph_o & 1u, kSiteEpilogue | kBarOFull) &&
+                          ptx::mbar_wait(wc, bars + 8 * kBarStFull, ph_t & 1u, kSiteEpilogue | kBarStFull);
+                if (has1)
                     ok = ok &&
-                         ptx::mbar_wait(wc, bars + 8 * (kBarOFull + h), ph_o & 1u, kSiteEpilogue | (kBarOFull + h)) &&
-                         ptx::mbar_wait(wc, bars + 8 * (kBarStFull + h), ph_t & 1u, kSiteEpilogue | (kBarStFull + h));
+                         ptx::mbar_wait(wc, bars + 8 * (kBarOFull + 1), (ph_o >> 1) & 1u, kSiteEpilogue | (kBarOFull + 1)) &&
+                         ptx::mbar_wait(wc, bars + 8 * (kBarStFull + 1), (ph_t >> 1) & 1u, kSiteEpilogue | (kBarStFull + 1));
                 ok = __all_sync(0xffffffffu, ok);
                 if (leader) go[0] = ok ? 1u : 0u;
             }
             ptx::named_bar_sync(1, 128);
             if (go[0] == 0u) goto done;
-            ph_o ^= 1u;
-            ph_t ^= 1u;
+            const uint32_t flip = has1 ? 3u : 1u;
+            ph_o ^= flip;
+            ph_t ^= flip;
             ptx::tc_fence_after();
-            const float4 s0 = stats[row], s1 = stats[kBM + row];
+            const float4 s0 = stats[row];
+            const float4 s1 = has1 ? stats[kBM + row] : make_float4(0.f, -INFINITY, 0.f, 0.f);
             __syncwarp();
             ptx::mbar_arrive(bars + 8 * kBarStEmpty, lane == 0);
-            ptx::mbar_arrive(bars + 8 * (kBarStEmpty + 1), lane == 0);
-            const float m = fmaxf(s0.y, s1.y);   // b0 is finite: key 0 of every unit is unmasked
-            const float w0 = ptx::ex2(s0.y - m), w1 = ptx::ex2(s1.y - m);
+            ptx::mbar_arrive(bars + 8 * (kBarStEmpty + 1), has1 && lane == 0);
+            const float m = fmaxf(s0.y, s1.y);   // b0 is finite: the unit's first key tile is unmasked for every row
+            const float w0 = ptx::ex2(s0.y - m), w1 = has1 ? ptx::ex2(s1.y - m) : 0.f;
             const float lsum = w0 * s0.x + w1 * s1.x;
             const float inv_l = 1.0f / (w0 * s0.z + w1 * s1.z);
             const float c0 = w0 * inv_l, c1 = w1 * inv_l;
             const float row_lse = (m + ptx::lg2(lsum)) * kLn2;
             const uint32_t tO0 = tmem + lane_base + C::col_o(0), tO1 = tmem + lane_base + C::col_o(1);
-            static_assert(D == 64, "key split: D=64");
+            static_assert(D == 64, "key-parity units: D=64");
             float osum = 0.f;   // converted V: a value beyond fp16's range makes O (and this sum) not finite
+            // O_0 and O_1, 32 columns at a time (O_1 only when slot 1 ran)
+            auto merged = [&](int c0c, uint32_t (&oa)[32], uint32_t (&ob)[32]) {
+                ptx::tmem_ld32(tO0 + c0c, oa);
+                if (has1) ptx::tmem_ld32(tO1 + c0c, ob);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence(oa);
+                ptx::reg_fence(ob);
+            };
             if constexpr (kSplit) {
                 const size_t slot = (size_t)un.id * kBM + row;   // one tile per unit
                 float* dst = p.ws_o + slot * D;
 #pragma unroll 1
                 for (int c0c = 0; c0c < D; c0c += 32) {
                     uint32_t oa[32], ob[32];
-                    ptx::tmem_ld32(tO0 + c0c, oa);
-                    ptx::tmem_ld32(tO1 + c0c, ob);
-                    ptx::tmem_wait_ld();
-                    ptx::reg_fence(oa);
-                    ptx::reg_fence(ob);
+                    merged(c0c, oa, ob);
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
                         float x[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            x[e] = fmaf(__uint_as_float(oa[i + e]), c0, __uint_as_float(ob[i + e]) * c1);
+                        for (int e2 = 0; e2 < 4; ++e2)
+                            x[e2] = has1 ? fmaf(__uint_as_float(oa[i + e2]), c0, __uint_as_float(ob[i + e2]) * c1)
+                                         : __uint_as_float(oa[i + e2]) * c0;
                         if constexpr (converts_v<kBF16>()) osum += (fabsf(x[0]) + fabsf(x[1])) + (fabsf(x[2]) + fabsf(x[3]));
                         *reinterpret_cast<float4*>(dst + c0c + i) = make_float4(x[0], x[1], x[2], x[3]);
                     }
@@ -710,7 +703,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                 ptx::tc_fence_before();
                 __syncwarp();
                 ptx::mbar_arrive(bars + 8 * kBarOEmpty, lane == 0);
-                ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1), lane == 0);
+                ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1), has1 && lane == 0);
                 continue;
             }
             const int qrow = un.q_tile[0] * kBM + row;
@@ -729,16 +722,14 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t oa[32], ob[32];
-                ptx::tmem_ld32(tO0 + half * 32, oa);
-                ptx::tmem_ld32(tO1 + half * 32, ob);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence(oa);
-                ptx::reg_fence(ob);
+                merged(half * 32, oa, ob);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float a = fmaf(__uint_as_float(oa[2 * i]), c0, __uint_as_float(ob[2 * i]) * c1);
-                    const float b2 = fmaf(__uint_as_float(oa[2 * i + 1]), c0, __uint_as_float(ob[2 * i + 1]) * c1);
+                    const float a = has1 ? fmaf(__uint_as_float(oa[2 * i]), c0, __uint_as_float(ob[2 * i]) * c1)
+                                         : __uint_as_float(oa[2 * i]) * c0;
+                    const float b2 = has1 ? fmaf(__uint_as_float(oa[2 * i + 1]), c0, __uint_as_float(ob[2 * i + 1]) * c1)
+                                          : __uint_as_float(oa[2 * i + 1]) * c0;
                     if constexpr (converts_v<kBF16>()) osum += fabsf(a) + fabsf(b2);
                     pk[i] = ptx::pack2<kBF16>(a, b2);
                 }
@@ -752,7 +743,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             ptx::tc_fence_before();
             __syncwarp();
             ptx::mbar_arrive(bars + 8 * kBarOEmpty, lane == 0);
-            ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1), lane == 0);
+            ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1), has1 && lane == 0);
             ptx::fence_proxy_async_shared();
             ptx::named_bar_sync(1, 128);
             if (leader) {
@@ -865,25 +856,25 @@ done:
 
 // ---------------------------------------------------------------------------------
 // TMA producer (one thread).
-template <int D, bool kSplit>
+template <int D, bool kSplit, bool kDec>
 __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& wc, const CUtensorMap* tm_q,
                                           const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t smem_base,
                                           uint32_t bars)
 {
     const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
-    using C = Cfg<D>;
+    using C = Cfg<D, kDec>;
     uint32_t ph_qe = 0u;       // phase bit of Q buffer t at bit t
     uint32_t q_issued = 0u;    // bit t: a Q load into buffer t was issued
     uint32_t kv_count = 0;
     bool ok = true;
     FA_TRACE_DECL;
     for (int r = 0; ok; ++r) {
-        const Unit un = unit_at<kSplit>(r, p);
+        const Unit un = unit_at<kSplit, kDec>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-            if (!ok || un.nkv[t] == 0) continue;
+            if (!ok || un.nkv[t] == 0 || (kDec && t == 1)) continue;   // key-parity units: one Q tile
             if (!ptx::mbar_wait(wc, bars + 8 * (kBarQEmpty + t), ((ph_qe >> t) & 1u) ^ 1u, kSiteLoad | (kBarQEmpty + t))) {
                 ok = false;
                 continue;
@@ -914,12 +905,18 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
                 }
                 ++kv_count;
                 const uint32_t fb = bars + 8 * (kBarKVFull + (C::kFullPairs ? (idx / 2u) % C::kPairs : slot));
-                ptx::mbar_arrive_expect_tx(fb, C::kTileBytes, ex);
-                const uint32_t dst = smem_base + C::kOffKV + slot * C::kTileBytes;
+                ptx::mbar_arrive_expect_tx(fb, C::kSlotBytes, ex);
+                const uint32_t dst = smem_base + C::kOffKV + slot * C::kSlotBytes;
                 const CUtensorMap* m = kind ? tm_v : tm_k;
+                // key-parity units: the step's two key tiles kt0 + 2j (slot 0)
+                // and kt0 + 2j + 1 (slot 1; past the sequence it is zero-filled)
 #pragma unroll
-                for (int bx = 0; bx < C::kBoxes; ++bx)
-                    ptx::tma_load_3d(m, dst + bx * C::kBoxBytes, fb, bx * 64, j * kBN, un.bh, ex);
+                for (int h = 0; h < (kDec ? 2 : 1); ++h) {
+                    const int row0 = (kDec ? un.kt0 + 2 * j + h : j) * kBN;
+#pragma unroll
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        ptx::tma_load_3d(m, dst + h * C::kTileBytes + bx * C::kBoxBytes, fb, bx * 64, row0, un.bh, ex);
+                }
                 FA_TRACE_EV(ex != 0u, kTrLoad, kEvKVLoad, idx);
             }
         }
@@ -956,15 +953,15 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
 // over units and key tiles is the loader's: K_j, then V_j, for every key tile
 // of every unit.  A value beyond fp16's range becomes infinite, so O does too;
 // the epilogues check O and record kSiteRangeV (no per-element check here).
-template <int D, bool kSplit, int kWarps>
+template <int D, bool kSplit, bool kDec, int kWarps>
 __device__ __forceinline__ void vconvert_role(const Params& p, const ptx::WaitCtx& wc, uint32_t smem_base,
                                               uint32_t bars, int conv_tid)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, kDec>;
     const int lane = threadIdx.x & 31;
     uint32_t kv_count = 0;
     for (int r = 0;; ++r) {
-        const Unit un = unit_at<kSplit>(r, p);
+        const Unit un = unit_at<kSplit, kDec>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         for (int j = un.j0; j < un.nmax; ++j) {
@@ -980,12 +977,12 @@ __device__ __forceinline__ void vconvert_role(const Params& p, const ptx::WaitCt
                                          kSiteLoad | 0x80u | (kBarKVFull + slot));
             }
             if (!ok) return;
-            const uint32_t tile = smem_base + C::kOffKV + (iv % C::kSlots) * C::kTileBytes;
+            const uint32_t tile = smem_base + C::kOffKV + (iv % C::kSlots) * C::kSlotBytes;
             // eight 16-byte chunks in flight per thread: the conversion's latency
             // sits in front of the tile's first P*V (unrolled 2: train 1088,
             // 8: 1152, 16: 1106 TFLOPS)
 #pragma unroll 8
-            for (uint32_t off = (uint32_t)conv_tid * 16u; off < (uint32_t)C::kTileBytes; off += 32u * kWarps * 16u) {
+            for (uint32_t off = (uint32_t)conv_tid * 16u; off < (uint32_t)C::kSlotBytes; off += 32u * kWarps * 16u) {
                 uint32_t w[4];
                 ptx::ld_shared_v4(tile + off, w);
 #pragma unroll
@@ -1007,10 +1004,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                                          uint32_t bars)
 {
     const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
-    using C = Cfg<D>;
+    using C = Cfg<D, kDec>;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);   // Q, K both K-major
     constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, p_is_bf16<kBF16>(), true);   // V MN-major (D contiguous)
-    static_assert(!kDec, "the decoupled instances issue from mma_role_ks");
     uint32_t ph_q = 0u, ph_ph = 0u, ph_p = 0u, ph_oe = 0u;   // phase bit of tile t at bit t
     uint32_t kv_count = 0;
     FA_TRACE_DECL;
@@ -1047,8 +1043,10 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     // (measured: +4.5% against rebuilding each descriptor).
     constexpr uint32_t kDescHi = ptx::sdesc_hi_sw128(1024);
     auto issue_qk = [&](int t, uint32_t idx) {
-        const uint32_t qa = ptx::sdesc_lo(smem_base + C::kOffQ + t * C::kTileBytes, 16);
-        const uint32_t kb = ptx::sdesc_lo(smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes, 16);
+        // key-parity units: one Q tile; slot t's key tile is the entry's t-th half
+        const uint32_t qa = ptx::sdesc_lo(smem_base + C::kOffQ + (kDec ? 0 : t) * C::kTileBytes, 16);
+        const uint32_t kb = ptx::sdesc_lo(
+            smem_base + C::kOffKV + (idx % C::kSlots) * C::kSlotBytes + (kDec ? t * C::kTileBytes : 0), 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
@@ -1061,18 +1059,18 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     // boxes kBoxBytes apart.
     // One half: keys 64*half .. 64*half+63 (four K=16 steps).
     auto issue_pv = [&](int t, uint32_t idx, int half, bool acc) {
-        const uint32_t vb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes;
+        const uint32_t vb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kSlotBytes + (kDec ? t * C::kTileBytes : 0);
         const uint32_t vl = ptx::sdesc_lo(vb, C::kBoxBytes);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = half * 4 + k4;
-            ptx::mma_ts(tmem + C::col_o(t), tmem + C::col_p(t, kDec) + kk * 8,
+            ptx::mma_ts(tmem + C::col_o(t), tmem + C::col_p(t) + kk * 8,
                         ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || kk > 0) ? 1u : 0u, ex);
         }
     };
 
     for (int r = 0;; ++r) {
-        const Unit un = unit_at<kSplit>(r, p);
+        const Unit un = unit_at<kSplit, kDec>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         // K_j is entry kvb + 2(j - j0) of the ring, V_j the entry after it
@@ -1082,11 +1080,17 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         // unit's very last QK and lands last, so QK_0 (and tile 0's softmax)
         // need not wait for it
         bool k_in = false;
+        // key-parity units read one Q buffer from both slots: it is released
+        // by the slot whose QK on it comes last in issue order
+        const int qe_slot = kDec ? (un.nkv[0] > un.nkv[1] ? 0 : 1) : 0;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (un.nkv[t] == 0) continue;
-            if (!ptx::mbar_wait(wc, bars + 8 * (kBarQFull + t), (ph_q >> t) & 1u, kSiteMma | (kBarQFull + t))) goto done;
-            ph_q ^= 1u << t;
+            if (!kDec || t == 0) {
+                if (!ptx::mbar_wait(wc, bars + 8 * (kBarQFull + t), (ph_q >> t) & 1u, kSiteMma | (kBarQFull + t)))
+                    goto done;
+                ph_q ^= 1u << t;
+            }
             if (!k_in) {
                 if (!kv_wait(kvb)) goto done;
                 k_in = true;
@@ -1095,7 +1099,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             issue_qk(t, kvb);
             ptx::mma_commit(bars + 8 * (kBarSFull + t), ex);
             FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, (uint32_t)t << 12);
-            if (un.nkv[t] == un.j0 + 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t), ex);
+            if (un.nkv[t] == un.j0 + 1 && (!kDec || t == qe_slot))
+                ptx::mma_commit(bars + 8 * (kBarQEmpty + (kDec ? 0 : t)), ex);
         }
         kv_release(kvb);
         for (int j = un.j0; j < un.nmax; ++j) {
@@ -1141,7 +1146,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     issue_qk(t, ik);
                     ptx::mma_commit(bars + 8 * (kBarSFull + t), ex);
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
-                    if (j + 1 == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarQEmpty + t), ex);
+                    if (j + 1 == un.nkv[t] - 1 && (!kDec || t == qe_slot))
+                        ptx::mma_commit(bars + 8 * (kBarQEmpty + (kDec ? 0 : t)), ex);
                 }
             }
             // V_j and K_{j+1} together; a unit's last V goes with the next
@@ -1157,138 +1163,13 @@ done:
 }
 
 // ---------------------------------------------------------------------------------
-// MMA issuer of the decoupled, key-split instances (one query tile per unit,
-// D=64): per key step j, QK(j+1) into S as soon as both warpgroups have read
-// S(j) (SFree_0, SFree_1), then PV_h(j) for each key half h once warpgroup h
-// has published its P: O_h += P[:, 64h .. 64h+63] V[64h .. 64h+63, :], four
-// K=16 MMAs from P_h's 32 TMEM columns.  Each PV_h commits PVDone_h (P_h and
-// O_h may then be rewritten).
-template <int D, bool kBF16, bool kSplit>
-__device__ __forceinline__ void mma_role_ks(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem, uint32_t smem_base,
-                                            uint32_t bars)
-{
-    const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
-    using C = Cfg<D>;
-    static_assert(C::kSepP && C::kFullPairs, "key split: D=64 layout");
-    constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);
-    constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, p_is_bf16<kBF16>(), true);
-    constexpr uint32_t kDescHi = ptx::sdesc_hi_sw128(1024);
-    uint32_t ph_q = 0u, ph_p = 0u, ph_oe = 0u, ph_sf = 0u;   // ph_p, ph_oe, ph_sf: bit h per key half
-    uint32_t kv_count = 0;
-    FA_TRACE_DECL;
-    // K_j and V_j land on one barrier at D=64: the wait for K_j also covers V_j
-    auto kv_wait = [&](uint32_t idx) -> bool {
-        const uint32_t q = idx / 2u, b = kBarKVFull + q % C::kPairs;
-        return ptx::mbar_wait(wc, bars + 8 * b, (q / C::kPairs) & 1u, kSiteMma | b);
-    };
-    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs), ex); };
-    auto s_free = [&]() -> bool {   // both warpgroups read the previous S
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (!ptx::mbar_wait(wc, bars + 8 * (kBarSFree + h), ((ph_sf >> h) & 1u) ^ 1u, kSiteMma | (kBarSFree + h)))
-                return false;
-            ph_sf ^= 1u << h;
-        }
-        return true;
-    };
-    const uint32_t qa = ptx::sdesc_lo(smem_base + C::kOffQ, 16);
-    auto issue_qk = [&](uint32_t idx) {
-        const uint32_t kb = ptx::sdesc_lo(smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes, 16);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            ptx::mma_ss(tmem + C::col_s(0), ptx::sdesc_join(qa + off, kDescHi), ptx::sdesc_join(kb + off, kDescHi),
-                        kIdescQK, kk > 0 ? 1u : 0u, ex);
-        }
-    };
-    auto issue_pv = [&](int h, uint32_t idx, bool acc) {
-        const uint32_t vl = ptx::sdesc_lo(smem_base + C::kOffKV + (idx % C::kSlots) * C::kTileBytes, C::kBoxBytes);
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const int kk = h * 4 + k4;   // key rows 16kk .. 16kk+15 of the tile
-            ptx::mma_ts(tmem + C::col_o(h), tmem + C::col_p(0, true) + kk * 8,
-                        ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || k4 > 0) ? 1u : 0u, ex);
-        }
-    };
-    auto v_wait = [&](uint32_t idx) -> bool {   // V_j converted (bf16 inputs)
-        if constexpr (converts_v<kBF16>()) {
-            const uint32_t slot = idx % C::kSlots;
-            return ptx::mbar_wait(wc, bars + 8 * (C::kBarVConv + slot), (idx / C::kSlots) & 1u,
-                                  kSiteMma | (C::kBarVConv + slot));
-        } else {
-            return true;
-        }
-    };
-
-    for (int r = 0;; ++r) {
-        const Unit un = unit_at<kSplit>(r, p);
-        if (un.status == kUnitDone) break;
-        if (un.status == kUnitSkip) continue;
-        const uint32_t kvb = kv_count;
-        const int nkv = un.nkv[0];
-        FA_TRACE_EV(ex != 0u, kTrMma, kEvUnit, un.id);
-        if (nkv > un.j0) {
-            if (!ptx::mbar_wait(wc, bars + 8 * kBarQFull, ph_q, kSiteMma | kBarQFull)) goto done;
-            ph_q ^= 1u;
-            if (!s_free() || !kv_wait(kvb)) goto done;
-            ptx::tc_fence_after();
-            issue_qk(kvb);
-            ptx::mma_commit(bars + 8 * kBarSFull, ex);
-            FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, un.j0);
-            if (nkv == un.j0 + 1) ptx::mma_commit(bars + 8 * kBarQEmpty, ex);
-        }
-        kv_release(kvb);
-        for (int j = un.j0; j < un.nmax; ++j) {
-            const uint32_t iv = kvb + 2 * (j - un.j0) + 1, ik = iv + 1;
-            if (j + 1 < nkv) {
-                if (!s_free() || !kv_wait(ik)) goto done;
-                ptx::tc_fence_after();
-                FA_TRACE_EV(ex != 0u, kTrMma, kEvQKGo, j + 1);
-                issue_qk(ik);
-                ptx::mma_commit(bars + 8 * kBarSFull, ex);
-                FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, j + 1);
-                if (j + 1 == nkv - 1) ptx::mma_commit(bars + 8 * kBarQEmpty, ex);
-            }
-            if (j < nkv) {
-                if (!v_wait(iv)) goto done;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPWait, ((uint32_t)h << 12) | j);
-                    if (!ptx::mbar_wait(wc, bars + 8 * (kBarPFull + h), (ph_p >> h) & 1u, kSiteMma | (kBarPFull + h)))
-                        goto done;
-                    ph_p ^= 1u << h;
-                    if (j == un.j0) {
-                        // O_h is overwritten: the previous unit's epilogue must have read it
-                        if (!ptx::mbar_wait(wc, bars + 8 * (kBarOEmpty + h), ((ph_oe >> h) & 1u) ^ 1u,
-                                            kSiteMma | (kBarOEmpty + h)))
-                            goto done;
-                        ph_oe ^= 1u << h;
-                    }
-                    ptx::tc_fence_after();
-                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPVGo, ((uint32_t)h << 12) | j);
-                    issue_pv(h, iv, j > un.j0);
-                    FA_TRACE_EV(ex != 0u, kTrMma, kEvPV, ((uint32_t)h << 12) | j);
-                    ptx::mma_commit(bars + 8 * (kBarPVDone + h), ex);   // P_h, O_h may be rewritten
-                    if (j == nkv - 1) ptx::mma_commit(bars + 8 * (kBarOFull + h), ex);
-                }
-            }
-            if (j + 1 < un.nmax) kv_release(ik);
-        }
-        kv_count = kvb + 2 * (un.nmax - un.j0);
-    }
-done:
-    ptx::mma_commit(bars + 8 * kBarDrain, ex);
-    ptx::mbar_wait_drain(wc, bars + 8 * kBarDrain, 0u, kSiteDrain | kBarDrain);
-}
-
-// ---------------------------------------------------------------------------------
 template <int D, bool kBF16, bool kSplit, bool kDec>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const __grid_constant__ Params p)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, kDec>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1316,8 +1197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars + 8 * (kBarOEmpty + t), 4);
             ptx::mbar_init(bars + 8 * (kBarStFull + t), 4);
             ptx::mbar_init(bars + 8 * (kBarStEmpty + t), 4);
-            ptx::mbar_init(bars + 8 * (kBarSFree + t), 4);
-            ptx::mbar_init(bars + 8 * (kBarPVDone + t), 1);
         }
         ptx::mbar_init(bars + 8 * kBarDrain, 1);
         for (int s = 0; s < C::kSlots; ++s) {
@@ -1356,7 +1235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < 12) {
         ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kEpilogue>();
         if constexpr (conv_warps<kBF16, kSplit, kDec>() == 6)
-            vconvert_role<D, kSplit, 6>(p, wc, base, bars, threadIdx.x - 8 * 32);
+            vconvert_role<D, kSplit, kDec, 6>(p, wc, base, bars, threadIdx.x - 8 * 32);
         else
             correction_epilogue_role<D, kBF16, kSplit, kDec>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
     } else {
@@ -1364,14 +1243,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the loader and the MMA issuer run on all 32 lanes of their warp (one
         // lane issues), so neither warp diverges while it waits
         if (warp == 12) {
-            load_role<D, kSplit>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
+            load_role<D, kSplit, kDec>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {
-            if constexpr (kDec) mma_role_ks<D, kBF16, kSplit>(p, wc, tmem, base, bars);
-            else mma_role<D, kBF16, kSplit, kDec>(p, wc, tmem, base, bars);
+            mma_role<D, kBF16, kSplit, kDec>(p, wc, tmem, base, bars);
         } else if constexpr (conv_warps<kBF16, kSplit, kDec>() == 6) {
-            vconvert_role<D, kSplit, 6>(p, wc, base, bars, 128 + threadIdx.x - 14 * 32);
+            vconvert_role<D, kSplit, kDec, 6>(p, wc, base, bars, 128 + threadIdx.x - 14 * 32);
         } else if constexpr (conv_warps<kBF16, kSplit, kDec>() == 2) {
-            vconvert_role<D, kSplit, 2>(p, wc, base, bars, threadIdx.x - 14 * 32);
+            vconvert_role<D, kSplit, kDec, 2>(p, wc, base, bars, threadIdx.x - 14 * 32);
         }
         __syncwarp();
     }
@@ -1393,14 +1271,14 @@ int launch_instance(const LaunchArgs& a, cudaStream_t stream)
     // on the first launch on each device only (it costs a driver call)
     cudaError_t e = cudaSuccess;
     if (!smem_opt_in_done(reinterpret_cast<const void*>(kern), a.device)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, kDec>::kSmemBytes);
         if (e != cudaSuccess) return (int)e;
         smem_opt_in_mark(reinterpret_cast<const void*>(kern), a.device);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+    cfg.dynamicSmemBytes = Cfg<D, kDec>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -55,9 +55,8 @@ def test_many_heads_two_tiles_per_unit(causal):
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_head_dim_64_one_tile_per_unit(dtype, causal):
-    # one query tile per unit: at D=64 this is the decoupled order (P in its
-    # own TMEM columns, the next QK issued before the PV); several key tiles
-    # and a ragged tail so the S-free / PV-done hand-offs cycle many times
+    # one query tile per unit: at D=64 its key tiles alternate between the two
+    # slots (key-parity units); many key tiles and a ragged tail
     for (B, H, S, seed) in [(1, 4, 1100, 11), (2, 3, 777, 12)]:
         assert _tiles_per_unit(B, H, S, 64, causal) == 1
         check_full(B, H, S, 64, dtype, causal, seed=seed)
@@ -65,12 +64,11 @@ def test_head_dim_64_one_tile_per_unit(dtype, causal):
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_head_dim_64_key_split_edges(dtype, causal):
-    # one tile per unit at D=64: the two warpgroups take keys 0-63 and 64-127
-    # of every key tile and the epilogue merges them; sequence ends on, just
-    # before and just after a half boundary, so one half is empty in the last
-    # tile (or, causal, in the first rows' only tile)
-    for S in (63, 64, 65, 191, 192, 193):
+def test_head_dim_64_key_parity_edges(dtype, causal):
+    # one tile per unit at D=64: the two slots take the query tile's even and
+    # odd key tiles and the epilogue merges them; sequences of one key tile
+    # (slot 1 absent), two, an odd count, and ragged tails in either slot
+    for S in (63, 128, 129, 256, 257, 383, 385):
         assert _tiles_per_unit(1, 2, S, 64, causal) == 1
         check_full(1, 2, S, 64, dtype, causal, seed=S)
 
