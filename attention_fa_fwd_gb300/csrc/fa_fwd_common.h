@@ -135,10 +135,10 @@ int launch_d64_f16_split(const LaunchArgs& a, cudaStream_t s);
 int launch_d64_bf16_split(const LaunchArgs& a, cudaStream_t s);
 int launch_d128_f16_split(const LaunchArgs& a, cudaStream_t s);
 int launch_d128_bf16_split(const LaunchArgs& a, cudaStream_t s);
-int launch_d64_f16_dec(const LaunchArgs& a, cudaStream_t s);
-int launch_d64_bf16_dec(const LaunchArgs& a, cudaStream_t s);
-int launch_d64_f16_split_dec(const LaunchArgs& a, cudaStream_t s);
-int launch_d64_bf16_split_dec(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_f16_kp(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_bf16_kp(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_f16_split_kp(const LaunchArgs& a, cudaStream_t s);
+int launch_d64_bf16_split_kp(const LaunchArgs& a, cudaStream_t s);
 
 // One-tile layout (fa_fwd_wide.cuh): one 128-row query tile per unit, steps of
 // kWideBN keys.  LaunchArgs::tm_o is not used; its K and V maps have boxes of

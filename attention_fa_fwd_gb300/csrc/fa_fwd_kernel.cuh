@@ -122,10 +122,10 @@ constexpr bool kEpilogueInSoftmax = FA_EPILOGUE_IN_SOFTMAX != 0;
 // epilogue warpgroup in the softmax warpgroups and all six warps converting
 // measured slower (train 1105 vs 1125, stress 1140 vs 1235 TFLOPS): the
 // conversion's cost is issue slots, not latency.
-template <bool kBF16, bool kSplit, bool kDec>
-__host__ __device__ constexpr bool epi_in_softmax() { return kEpilogueInSoftmax && !kSplit && !kDec; }
-template <bool kBF16, bool kSplit, bool kDec>
-__host__ __device__ constexpr int conv_warps() { return converts_v<kBF16>() ? (epi_in_softmax<kBF16, kSplit, kDec>() ? 6 : 2) : 0; }
+template <bool kBF16, bool kSplit, bool kKP>
+__host__ __device__ constexpr bool epi_in_softmax() { return kEpilogueInSoftmax && !kSplit && !kKP; }
+template <bool kBF16, bool kSplit, bool kKP>
+__host__ __device__ constexpr int conv_warps() { return converts_v<kBF16>() ? (epi_in_softmax<kBF16, kSplit, kKP>() ? 6 : 2) : 0; }
 static_assert(kExp2PolyPairs >= 0 && kExp2PolyPairs <= 16, "FA_EXP2_POLY_PAIRS must be in [0, 16]");
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -133,23 +133,23 @@ constexpr float kLn2 = 0.693147180559945309f;
 // (load + MMA).  The four add up to 512 = 65536 registers / 128 threads; the
 // splits are the spill-free ones ptxas -v reports for each head dim and type
 //
-template <int D, bool kBF16, bool kSplit, bool kDec> struct RegSplit {   // D=128 one pass, D=64 split-KV
+template <int D, bool kBF16, bool kSplit, bool kKP> struct RegSplit {   // D=128 one pass, D=64 split-KV
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 56, kControl = 88;
 };
-template <bool kBF16, bool kDec> struct RegSplit<64, kBF16, false, kDec> {
+template <bool kBF16, bool kKP> struct RegSplit<64, kBF16, false, kKP> {
     static constexpr uint32_t kSoftmax = 184, kEpilogue = 72, kControl = 72;
 };
-// key-parity units (kDec): the epilogue merges two accumulators
+// key-parity units (kKP): the epilogue merges two accumulators
 template <bool kBF16> struct RegSplit<64, kBF16, false, true> {
     static constexpr uint32_t kSoftmax = 176, kEpilogue = 88, kControl = 72;
 };
 template <bool kBF16> struct RegSplit<64, kBF16, true, true> {
     static constexpr uint32_t kSoftmax = 176, kEpilogue = 88, kControl = 72;
 };
-template <int D, bool kBF16, bool kSplit, bool kDec>
+template <int D, bool kBF16, bool kSplit, bool kKP>
 constexpr bool reg_split_fits()
 {
-    using R = RegSplit<D, kBF16, kSplit, kDec>;
+    using R = RegSplit<D, kBF16, kSplit, kKP>;
     return 2 * R::kSoftmax + R::kEpilogue + R::kControl == 512;
 }
 static_assert(reg_split_fits<128, false, false, false>() && reg_split_fits<128, false, true, false>() &&
@@ -387,14 +387,14 @@ enum : uint32_t { kSiteSoftmax = 0x100, kSiteEpilogue = 0x300, kSiteLoad = 0x400
 
 // ---------------------------------------------------------------------------------
 // Softmax warpgroup t: one thread per query row of tile t.
-template <int D, bool kBF16, bool kSplit, bool kDec>
+template <int D, bool kBF16, bool kSplit, bool kKP>
 __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx& wc, int t, uint32_t tmem,
                                              uint32_t bars, float4* stats)
 {
-    // kDec: key-parity units (one query tile; slot t takes its key tiles
+    // kKP: key-parity units (one query tile; slot t takes its key tiles
     // kt0 + 2j + t, with its own base, sum and accumulator O_t, merged by the
     // epilogue).  Otherwise slot t is query tile t of the unit.
-    using C = Cfg<D, kDec>;
+    using C = Cfg<D, kKP>;
     const int lane = threadIdx.x & 31;
     const int wq = (threadIdx.x >> 5) & 3;
     const int row = wq * 32 + lane;
@@ -408,14 +408,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
     const bool tr = (threadIdx.x & 127) == 0;
 
     for (int r = 0;; ++r) {
-        const Unit un = unit_at<kSplit, kDec>(r, p);
+        const Unit un = unit_at<kSplit, kKP>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         // t is a runtime value: select instead of indexing, so the unit stays in registers
         const int nkv = t ? un.nkv[1] : un.nkv[0];
         const int q_tile = t ? un.q_tile[1] : un.q_tile[0];
         // the masked tile: the row's last key tile (always nkv - 1 without a split)
-        const int last = (kSplit || kDec) ? (t ? un.last[1] : un.last[0]) : nkv - 1;
+        const int last = (kSplit || kKP) ? (t ? un.last[1] : un.last[0]) : nkv - 1;
         if (nkv == 0) continue;
         float b = -INFINITY;   // base of the row, base-2 scaled units
         float l = 0.f;         // running sum of 2^(x - b): gives the LSE
@@ -428,7 +428,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
         // 1.1e-3 off).  fp16 inputs round O to 2^-11 relative: dl stays 0.
         float dl = 0.f;
         for (int j = un.j0; j < nkv; ++j) {
-            const int kt = kDec ? un.kt0 + 2 * j + t : j;   // the key tile in S_t
+            const int kt = kKP ? un.kt0 + 2 * j + t : j;   // the key tile in S_t
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + t), ph_s, kSiteSoftmax | (kBarSFull + t))) return;
             ph_s ^= 1u;
             FA_TRACE_EV(tr, t, kEvSReady, j);
@@ -552,7 +552,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             l = fmaf(l, h, sa + sb);
         }
 #ifdef FA_DEBUG_STATS
-        if (!kSplit && !kDec && p.dbg_rows != nullptr) {
+        if (!kSplit && !kKP && p.dbg_rows != nullptr) {
             // the debug build writes each row's final base and row sum
             const int qrow = q_tile * kBM + row;
             if (qrow < p.S) {
@@ -562,7 +562,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             }
         }
 #endif
-        if constexpr (epi_in_softmax<kBF16, kSplit, kDec>()) {
+        if constexpr (epi_in_softmax<kBF16, kSplit, kKP>()) {
             // this tile's epilogue, here: O_t is final once its last PV completed
             if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarOFull + t), ph_o, kSiteSoftmax | (kBarOFull + t))) return;
             ph_o ^= 1u;
@@ -612,12 +612,12 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
 // ---------------------------------------------------------------------------------
 // Correction/epilogue warpgroup: per unit and query tile, the final correction
 // O_t / l, the LSE, conversion to 16 bits, shared-memory staging, TMA store.
-template <int D, bool kBF16, bool kSplit, bool kDec>
+template <int D, bool kBF16, bool kSplit, bool kKP>
 __device__ __forceinline__ void correction_epilogue_role(const Params& p, const ptx::WaitCtx& wc,
                                                          const CUtensorMap* tm_o, uint32_t tmem, uint32_t smem_base,
                                                          uint32_t bars, const float4* stats, volatile uint32_t* ctl_go)
 {
-    using C = Cfg<D, kDec>;
+    using C = Cfg<D, kKP>;
     const int lane = threadIdx.x & 31;
     const int wq = (threadIdx.x >> 5) & 3;
     const int row = wq * 32 + lane;
@@ -627,13 +627,13 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
     volatile uint32_t* go = ctl_go;   // leader's wait outcome, read by all 128 threads
     uint32_t ph_o = 0u, ph_t = 0u;   // phase bit of tile t at bit t
     FA_TRACE_DECL;
-    if constexpr (epi_in_softmax<kBF16, kSplit, kDec>()) return;   // the softmax warpgroups run the epilogue
+    if constexpr (epi_in_softmax<kBF16, kSplit, kKP>()) return;   // the softmax warpgroups run the epilogue
 
     for (int r = 0;; ++r) {
-        const Unit un = unit_at<kSplit, kDec>(r, p);
+        const Unit un = unit_at<kSplit, kKP>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
-        if constexpr (kDec) {
+        if constexpr (kKP) {
             // key-parity unit: the unit's one query tile has two partial
             // results, slot 0 (its even key tiles: O_0, base b0, sum l0) and
             // slot 1 (odd: O_1, b1, l1; absent when the unit has one key tile);
@@ -856,25 +856,25 @@ done:
 
 // ---------------------------------------------------------------------------------
 // TMA producer (one thread).
-template <int D, bool kSplit, bool kDec>
+template <int D, bool kSplit, bool kKP>
 __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& wc, const CUtensorMap* tm_q,
                                           const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t smem_base,
                                           uint32_t bars)
 {
     const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
-    using C = Cfg<D, kDec>;
+    using C = Cfg<D, kKP>;
     uint32_t ph_qe = 0u;       // phase bit of Q buffer t at bit t
     uint32_t q_issued = 0u;    // bit t: a Q load into buffer t was issued
     uint32_t kv_count = 0;
     bool ok = true;
     FA_TRACE_DECL;
     for (int r = 0; ok; ++r) {
-        const Unit un = unit_at<kSplit, kDec>(r, p);
+        const Unit un = unit_at<kSplit, kKP>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-            if (!ok || un.nkv[t] == 0 || (kDec && t == 1)) continue;   // key-parity units: one Q tile
+            if (!ok || un.nkv[t] == 0 || (kKP && t == 1)) continue;   // key-parity units: one Q tile
             if (!ptx::mbar_wait(wc, bars + 8 * (kBarQEmpty + t), ((ph_qe >> t) & 1u) ^ 1u, kSiteLoad | (kBarQEmpty + t))) {
                 ok = false;
                 continue;
@@ -911,8 +911,8 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
                 // key-parity units: the step's two key tiles kt0 + 2j (slot 0)
                 // and kt0 + 2j + 1 (slot 1; past the sequence it is zero-filled)
 #pragma unroll
-                for (int h = 0; h < (kDec ? 2 : 1); ++h) {
-                    const int row0 = (kDec ? un.kt0 + 2 * j + h : j) * kBN;
+                for (int h = 0; h < (kKP ? 2 : 1); ++h) {
+                    const int row0 = (kKP ? un.kt0 + 2 * j + h : j) * kBN;
 #pragma unroll
                     for (int bx = 0; bx < C::kBoxes; ++bx)
                         ptx::tma_load_3d(m, dst + h * C::kTileBytes + bx * C::kBoxBytes, fb, bx * 64, row0, un.bh, ex);
@@ -953,15 +953,15 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
 // over units and key tiles is the loader's: K_j, then V_j, for every key tile
 // of every unit.  A value beyond fp16's range becomes infinite, so O does too;
 // the epilogues check O and record kSiteRangeV (no per-element check here).
-template <int D, bool kSplit, bool kDec, int kWarps>
+template <int D, bool kSplit, bool kKP, int kWarps>
 __device__ __forceinline__ void vconvert_role(const Params& p, const ptx::WaitCtx& wc, uint32_t smem_base,
                                               uint32_t bars, int conv_tid)
 {
-    using C = Cfg<D, kDec>;
+    using C = Cfg<D, kKP>;
     const int lane = threadIdx.x & 31;
     uint32_t kv_count = 0;
     for (int r = 0;; ++r) {
-        const Unit un = unit_at<kSplit, kDec>(r, p);
+        const Unit un = unit_at<kSplit, kKP>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         for (int j = un.j0; j < un.nmax; ++j) {
@@ -999,12 +999,12 @@ __device__ __forceinline__ void vconvert_role(const Params& p, const ptx::WaitCt
 
 // ---------------------------------------------------------------------------------
 // tcgen05 MMA issuer (one thread).
-template <int D, bool kBF16, bool kSplit, bool kDec>
+template <int D, bool kBF16, bool kSplit, bool kKP>
 __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc, uint32_t tmem, uint32_t smem_base,
                                          uint32_t bars)
 {
     const uint32_t ex = (threadIdx.x & 31) == 0 ? 1u : 0u;   // the lane that issues (the whole warp runs the role)
-    using C = Cfg<D, kDec>;
+    using C = Cfg<D, kKP>;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);   // Q, K both K-major
     constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, p_is_bf16<kBF16>(), true);   // V MN-major (D contiguous)
     uint32_t ph_q = 0u, ph_ph = 0u, ph_p = 0u, ph_oe = 0u;   // phase bit of tile t at bit t
@@ -1044,9 +1044,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     constexpr uint32_t kDescHi = ptx::sdesc_hi_sw128(1024);
     auto issue_qk = [&](int t, uint32_t idx) {
         // key-parity units: one Q tile; slot t's key tile is the entry's t-th half
-        const uint32_t qa = ptx::sdesc_lo(smem_base + C::kOffQ + (kDec ? 0 : t) * C::kTileBytes, 16);
+        const uint32_t qa = ptx::sdesc_lo(smem_base + C::kOffQ + (kKP ? 0 : t) * C::kTileBytes, 16);
         const uint32_t kb = ptx::sdesc_lo(
-            smem_base + C::kOffKV + (idx % C::kSlots) * C::kSlotBytes + (kDec ? t * C::kTileBytes : 0), 16);
+            smem_base + C::kOffKV + (idx % C::kSlots) * C::kSlotBytes + (kKP ? t * C::kTileBytes : 0), 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
@@ -1059,7 +1059,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     // boxes kBoxBytes apart.
     // One half: keys 64*half .. 64*half+63 (four K=16 steps).
     auto issue_pv = [&](int t, uint32_t idx, int half, bool acc) {
-        const uint32_t vb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kSlotBytes + (kDec ? t * C::kTileBytes : 0);
+        const uint32_t vb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kSlotBytes + (kKP ? t * C::kTileBytes : 0);
         const uint32_t vl = ptx::sdesc_lo(vb, C::kBoxBytes);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
@@ -1070,7 +1070,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     };
 
     for (int r = 0;; ++r) {
-        const Unit un = unit_at<kSplit, kDec>(r, p);
+        const Unit un = unit_at<kSplit, kKP>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
         // K_j is entry kvb + 2(j - j0) of the ring, V_j the entry after it
@@ -1082,11 +1082,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         bool k_in = false;
         // key-parity units read one Q buffer from both slots: it is released
         // by the slot whose QK on it comes last in issue order
-        const int qe_slot = kDec ? (un.nkv[0] > un.nkv[1] ? 0 : 1) : 0;
+        const int qe_slot = kKP ? (un.nkv[0] > un.nkv[1] ? 0 : 1) : 0;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (un.nkv[t] == 0) continue;
-            if (!kDec || t == 0) {
+            if (!kKP || t == 0) {
                 if (!ptx::mbar_wait(wc, bars + 8 * (kBarQFull + t), (ph_q >> t) & 1u, kSiteMma | (kBarQFull + t)))
                     goto done;
                 ph_q ^= 1u << t;
@@ -1099,8 +1099,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             issue_qk(t, kvb);
             ptx::mma_commit(bars + 8 * (kBarSFull + t), ex);
             FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, (uint32_t)t << 12);
-            if (un.nkv[t] == un.j0 + 1 && (!kDec || t == qe_slot))
-                ptx::mma_commit(bars + 8 * (kBarQEmpty + (kDec ? 0 : t)), ex);
+            if (un.nkv[t] == un.j0 + 1 && (!kKP || t == qe_slot))
+                ptx::mma_commit(bars + 8 * (kBarQEmpty + (kKP ? 0 : t)), ex);
         }
         kv_release(kvb);
         for (int j = un.j0; j < un.nmax; ++j) {
@@ -1146,8 +1146,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     issue_qk(t, ik);
                     ptx::mma_commit(bars + 8 * (kBarSFull + t), ex);
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
-                    if (j + 1 == un.nkv[t] - 1 && (!kDec || t == qe_slot))
-                        ptx::mma_commit(bars + 8 * (kBarQEmpty + (kDec ? 0 : t)), ex);
+                    if (j + 1 == un.nkv[t] - 1 && (!kKP || t == qe_slot))
+                        ptx::mma_commit(bars + 8 * (kBarQEmpty + (kKP ? 0 : t)), ex);
                 }
             }
             // V_j and K_{j+1} together; a unit's last V goes with the next
@@ -1163,13 +1163,13 @@ done:
 }
 
 // ---------------------------------------------------------------------------------
-template <int D, bool kBF16, bool kSplit, bool kDec>
+template <int D, bool kBF16, bool kSplit, bool kKP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const __grid_constant__ Params p)
 {
-    using C = Cfg<D, kDec>;
+    using C = Cfg<D, kKP>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1202,7 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kSlots; ++s) {
             ptx::mbar_init(bars + 8 * (kBarKVFull + s), C::kFullPairs ? 2 : 1);   // (K_j's and V_j's copies)
             ptx::mbar_init(bars + 8 * (C::kBarKVEmpty + s), 1);
-            ptx::mbar_init(bars + 8 * (C::kBarVConv + s), conv_warps<kBF16, kSplit, kDec>() > 0 ? conv_warps<kBF16, kSplit, kDec>() : 1);
+            ptx::mbar_init(bars + 8 * (C::kBarVConv + s), conv_warps<kBF16, kSplit, kKP>() > 0 ? conv_warps<kBF16, kSplit, kKP>() : 1);
         }
         ctl[1] = 0u;
         ptx::fence_mbar_init();
@@ -1230,26 +1230,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     FA_TRACE_EV(threadIdx.x == 0, kTrKernel, kEvSetup, 0);
 
     if (warp < 8) {
-        ptx::setmaxnreg_inc<RegSplit<D, kBF16, kSplit, kDec>::kSoftmax>();
-        softmax_role<D, kBF16, kSplit, kDec>(p, wc, warp >> 2, tmem, bars, stats);
+        ptx::setmaxnreg_inc<RegSplit<D, kBF16, kSplit, kKP>::kSoftmax>();
+        softmax_role<D, kBF16, kSplit, kKP>(p, wc, warp >> 2, tmem, bars, stats);
     } else if (warp < 12) {
-        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kEpilogue>();
-        if constexpr (conv_warps<kBF16, kSplit, kDec>() == 6)
-            vconvert_role<D, kSplit, kDec, 6>(p, wc, base, bars, threadIdx.x - 8 * 32);
+        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kKP>::kEpilogue>();
+        if constexpr (conv_warps<kBF16, kSplit, kKP>() == 6)
+            vconvert_role<D, kSplit, kKP, 6>(p, wc, base, bars, threadIdx.x - 8 * 32);
         else
-            correction_epilogue_role<D, kBF16, kSplit, kDec>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
+            correction_epilogue_role<D, kBF16, kSplit, kKP>(p, wc, &tm_o, tmem, base, bars, stats, ctl + 2);
     } else {
-        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kDec>::kControl>();
+        ptx::setmaxnreg_dec<RegSplit<D, kBF16, kSplit, kKP>::kControl>();
         // the loader and the MMA issuer run on all 32 lanes of their warp (one
         // lane issues), so neither warp diverges while it waits
         if (warp == 12) {
-            load_role<D, kSplit, kDec>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
+            load_role<D, kSplit, kKP>(p, wc, &tm_q, &tm_k, &tm_v, base, bars);
         } else if (warp == 13) {
-            mma_role<D, kBF16, kSplit, kDec>(p, wc, tmem, base, bars);
-        } else if constexpr (conv_warps<kBF16, kSplit, kDec>() == 6) {
-            vconvert_role<D, kSplit, kDec, 6>(p, wc, base, bars, 128 + threadIdx.x - 14 * 32);
-        } else if constexpr (conv_warps<kBF16, kSplit, kDec>() == 2) {
-            vconvert_role<D, kSplit, kDec, 2>(p, wc, base, bars, threadIdx.x - 14 * 32);
+            mma_role<D, kBF16, kSplit, kKP>(p, wc, tmem, base, bars);
+        } else if constexpr (conv_warps<kBF16, kSplit, kKP>() == 6) {
+            vconvert_role<D, kSplit, kKP, 6>(p, wc, base, bars, 128 + threadIdx.x - 14 * 32);
+        } else if constexpr (conv_warps<kBF16, kSplit, kKP>() == 2) {
+            vconvert_role<D, kSplit, kKP, 2>(p, wc, base, bars, threadIdx.x - 14 * 32);
         }
         __syncwarp();
     }
@@ -1263,22 +1263,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool kBF16, bool kSplit, bool kDec = false>
+template <int D, bool kBF16, bool kSplit, bool kKP = false>
 int launch_instance(const LaunchArgs& a, cudaStream_t stream)
 {
-    auto kern = fa_fwd_kernel<D, kBF16, kSplit, kDec>;
+    auto kern = fa_fwd_kernel<D, kBF16, kSplit, kKP>;
     // the shared-memory opt-in is a per-device property of the kernel: set it
     // on the first launch on each device only (it costs a driver call)
     cudaError_t e = cudaSuccess;
     if (!smem_opt_in_done(reinterpret_cast<const void*>(kern), a.device)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, kDec>::kSmemBytes);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, kKP>::kSmemBytes);
         if (e != cudaSuccess) return (int)e;
         smem_opt_in_mark(reinterpret_cast<const void*>(kern), a.device);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<D, kDec>::kSmemBytes;
+    cfg.dynamicSmemBytes = Cfg<D, kKP>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -1,4 +1,4 @@
-// Kernel instance: head dim 128, bf16 inputs/outputs, one pass (no key split).
+// Kernel instance: head dim 128, bf16 inputs/outputs, one pass (no split of the key range).
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {

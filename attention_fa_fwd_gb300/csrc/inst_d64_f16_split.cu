@@ -4,7 +4,7 @@
 namespace fa {
 int launch_d64_f16_split(const LaunchArgs& a, cudaStream_t s)
 {
-    if (a.p.tpu == 1) return launch_d64_f16_split_dec(a, s);
+    if (a.p.tpu == 1) return launch_d64_f16_split_kp(a, s);
     return launch_instance<64, false, true>(a, s);
 }
 }  // namespace fa
