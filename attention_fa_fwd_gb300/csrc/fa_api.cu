@@ -695,8 +695,11 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
             e = dtype == FA_DTYPE_BF16 ? fa::launch_wide_d128_bf16(a, s) : fa::launch_wide_d128_f16(a, s);
         return e == (int)cudaSuccess ? FA_OK : FA_ERR_CUDA;
     }
-    if (make_tmap(&a.tm_q, q, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_k, k, BH, S, D, dtype) != FA_OK ||
-        make_tmap(&a.tm_v, v, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_o, o, BH, S, D, dtype) != FA_OK)
+    // key-parity units (D=64, one query tile per unit) load a step's two key
+    // tiles with one 256-row copy
+    const int kv_rows = (D == 64 && a.p.tpu == 1) ? 2 * kBM : kBM;
+    if (make_tmap(&a.tm_q, q, BH, S, D, dtype) != FA_OK || make_tmap(&a.tm_k, k, BH, S, D, dtype, kv_rows) != FA_OK ||
+        make_tmap(&a.tm_v, v, BH, S, D, dtype, kv_rows) != FA_OK || make_tmap(&a.tm_o, o, BH, S, D, dtype) != FA_OK)
         return FA_ERR_CUDA;
 
     if (D == 64)

@@ -910,13 +910,11 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
                 const CUtensorMap* m = kind ? tm_v : tm_k;
                 // key-parity units: the step's two key tiles kt0 + 2j (slot 0)
                 // and kt0 + 2j + 1 (slot 1; past the sequence it is zero-filled)
+                // in one 256-row copy (their tensor maps have 256-row boxes)
+                const int row0 = (kKP ? un.kt0 + 2 * j : j) * kBN;
 #pragma unroll
-                for (int h = 0; h < (kKP ? 2 : 1); ++h) {
-                    const int row0 = (kKP ? un.kt0 + 2 * j + h : j) * kBN;
-#pragma unroll
-                    for (int bx = 0; bx < C::kBoxes; ++bx)
-                        ptx::tma_load_3d(m, dst + h * C::kTileBytes + bx * C::kBoxBytes, fb, bx * 64, row0, un.bh, ex);
-                }
+                for (int bx = 0; bx < C::kBoxes; ++bx)
+                    ptx::tma_load_3d(m, dst + bx * C::kBoxBytes, fb, bx * 64, row0, un.bh, ex);
                 FA_TRACE_EV(ex != 0u, kTrLoad, kEvKVLoad, idx);
             }
         }
