@@ -31,7 +31,9 @@
 // MMA issue order per key tile j ("G6", V39, interleave):
 //   PV0(j), QK0(j+1), PV1(j), QK1(j+1)
 // so the tensor core computes one tile's scores while the other tile's softmax
-// runs.  Each PV is issued in two halves (keys 0-63, then 64-127): the softmax
+// runs (the FA_SCORE_ROTATION build option issues QK(j+1) earlier still at
+// D=64, into a third score buffer; see Cfg::kRot).  Each PV is issued in two
+// halves (keys 0-63, then 64-127): the softmax
 // publishes the first half of P before it computes the second ("G6", V43, PV
 // split), so half of P*V overlaps the second half of the exponentials.
 //
@@ -126,6 +128,14 @@ template <bool kBF16, bool kSplit, bool kKP>
 __host__ __device__ constexpr bool epi_in_softmax() { return kEpilogueInSoftmax && !kSplit && !kKP; }
 template <bool kBF16, bool kSplit, bool kKP>
 __host__ __device__ constexpr int conv_warps() { return converts_v<kBF16>() ? (epi_in_softmax<kBF16, kSplit, kKP>() ? 6 : 2) : 0; }
+// Three rotating score buffers at D=64 (Cfg::kRot): each slot's next scores
+// are computed while its softmax still works on the current ones.  Off by
+// default: the hand-off chain they remove is not what bounds the D=64
+// launches (measured slower, the build option exists to measure that).
+#ifndef FA_SCORE_ROTATION
+#define FA_SCORE_ROTATION 0
+#endif
+constexpr bool kScoreRotation = FA_SCORE_ROTATION != 0;
 static_assert(kExp2PolyPairs >= 0 && kExp2PolyPairs <= 16, "FA_EXP2_POLY_PAIRS must be in [0, 16]");
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -157,19 +167,29 @@ static_assert(reg_split_fits<128, false, false, false>() && reg_split_fits<128, 
                   reg_split_fits<64, false, true, false>() && reg_split_fits<64, false, true, true>(),
               "register split must add up to 512");
 
-// Barrier indices inside the barrier array.
+// Barrier indices inside the barrier array.  The score and P barriers come in
+// kStepBars per tile slot, taken in turn by the slot's key steps with
+// FA_SCORE_ROTATION (Cfg::kRot), else only the slot's first one.  The spacing
+// matters without the rotation too: with the two slots' score, P-half and
+// P-full barriers adjacent (one 16-byte chunk per pair) the D=128 launches ran
+// 1.5% (4x32x4096) and 3% (1x32x16384) slower than with these 24-byte gaps;
+// wider gaps (16, 32 or 128 bytes per barrier) measured no better.
+constexpr int kStepBars = 3;
+// Bytes from one barrier to the next in shared memory.
+constexpr uint32_t kBarStride = 8;
 enum : int {
     kBarQFull = 0,      // [2] Q tile t landed (TMA tx)
     kBarQEmpty = 2,     // [2] last QK of tile t finished (commit)
-    kBarSFull = 4,      // [2] scores S_t ready (commit)
-    kBarPHalf = 6,      // [2] P_t keys 0-63 in TMEM, O_t rescaled (4 softmax warps)
-    kBarPFull = 8,      // [2] P_t keys 64-127 in TMEM (4 softmax warps)
-    kBarOFull = 10,     // [2] last PV of tile t finished (commit)
-    kBarOEmpty = 12,    // [2] epilogue done reading O_t (4 epilogue warps)
-    kBarStFull = 14,    // [2] row statistics of tile t in shared memory (4 softmax warps)
-    kBarStEmpty = 16,   // [2] epilogue took the statistics (4 epilogue warps)
-    kBarDrain = 18,     // MMA drain at exit (commit)
-    kBarKVFull = 19,    // [slots] K or V tile landed (TMA tx)
+    kBarSFull = 4,      // [2][kStepBars] scores of slot t's step ready (commit)
+    kBarPHalf = 10,     // [2][kStepBars] P keys 0-63 in TMEM, O_t rescaled (4 softmax warps)
+    kBarPFull = 16,     // [2][kStepBars] P keys 64-127 in TMEM (4 softmax warps)
+    kBarOFull = 22,     // [2] last PV of tile t finished (commit)
+    kBarOEmpty = 24,    // [2] epilogue done reading O_t (4 epilogue warps)
+    kBarStFull = 26,    // [2] row statistics of tile t in shared memory (4 softmax warps)
+    kBarStEmpty = 28,   // [2] epilogue took the statistics (4 epilogue warps)
+    kBarPVDone = 30,    // [2][2] a P*V of slot t that is not the unit's last finished (commit)
+    kBarDrain = 34,     // MMA drain at exit (commit)
+    kBarKVFull = 35,    // [slots] K or V tile landed (TMA tx)
 };
 
 template <int D, bool kKP = false>
@@ -198,7 +218,7 @@ struct Cfg {
     // 8-slot ring there is slack for it, with D=128's 4 slots there is not
     // (measured 5-9% slower there, 2-3% faster at D=64).  kSlots barriers are
     // reserved per side.
-    static constexpr bool kFullPairs = (D == 64);
+    static constexpr bool kFullPairs = (D == 64) && !(kKP && kScoreRotation);
     static constexpr int kPairs = kSlots / 2;
     static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
     __device__ static constexpr uint32_t pair_of(uint32_t entry) { return (entry + 1u) / 2u; }
@@ -208,16 +228,27 @@ struct Cfg {
     static constexpr int kBarVConv = kBarKVEmpty + kSlots;
     static constexpr int kNumBars = kBarVConv + kSlots;
     static constexpr int kOffBars = kOffStats + 2 * kBM * 16;
-    static constexpr int kOffCtl = kOffBars + kNumBars * 8;          // [0] TMEM base, [1] abort, [2] epilogue go
+    static constexpr int kOffCtl = kOffBars + kNumBars * (int)kBarStride;          // [0] TMEM base, [1] abort, [2] epilogue go
     static constexpr int kSmemBytes = kOffCtl + 16 + 1024;            // + slack to align the base to 1 KB
-    // TMEM columns: S0 | S1 | O0 | O1.  P_t overwrites the first half of S_t,
-    // so the next QK_t must wait for PV_t (the issuer orders them).  In
-    // key-parity units the two slots hold one query tile's even and odd key
-    // tiles: O0 and O1 are two partial accumulators the epilogue merges.
+    // TMEM columns.  D=128: S0 | S1 | O0 | O1; P_t overwrites the first half of
+    // S_t, so the next QK_t must wait for PV_t (the issuer orders them).
+    // D=64 (kRot): three score buffers SB0 | SB1 | SB2 and O0 | O1 fill the 512
+    // columns.  A unit's key steps, slot by slot in issue order, are its ops
+    // 0, 1, 2, ...; op m's scores (and then its P) live in buffer m % 3, and
+    // the QK of op m + 3 is issued right after the PV of op m, so each slot's
+    // next scores are computed while its softmax still works on the current
+    // ones (with two buffers they could only follow the PV).  In key-parity
+    // units the two slots hold one query tile's even and odd key tiles: O0
+    // and O1 are two partial accumulators the epilogue merges.
+    static constexpr bool kRot = (D == 64) && kScoreRotation;
+    static constexpr int kSBufs = kRot ? 3 : 2;
+    static_assert(kSBufs <= kStepBars, "one step barrier per score buffer");
     __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
-    __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
+    __device__ static constexpr uint32_t col_sb(uint32_t b) { return 128u * b; }
+    __device__ static constexpr uint32_t col_o(int t) { return (kRot ? 384u : 256u) + (t ? (uint32_t)D : 0u); }
     __device__ static constexpr uint32_t col_p(int t) { return col_s(t); }
 };
+
 
 static_assert(Cfg<64, true>::kSmemBytes <= Cfg<64>::kSmemBytes, "key-parity instances fit the D=64 launch geometry");
 
@@ -234,6 +265,27 @@ struct Unit {
 };
 
 enum : int { kUnitDone = 0, kUnitOk = 1, kUnitSkip = 2 };
+
+// A unit's ops (kRot): the key steps of its two slots in issue order.  While
+// both slots have steps left, op 2i is slot 0's step j0 + i and op 2i + 1 slot
+// 1's; after that the slot with more steps runs alone.
+struct OpMap {
+    int j0, cm, tl, n;   // first step, steps both slots run, the longer slot, op count
+    __device__ __forceinline__ OpMap(const Unit& un) {
+        const int c0 = un.nkv[0] > un.j0 ? un.nkv[0] - un.j0 : 0;
+        const int c1 = un.nkv[1] > un.j0 ? un.nkv[1] - un.j0 : 0;
+        j0 = un.j0;
+        cm = min(c0, c1);
+        tl = c0 > c1 ? 0 : 1;
+        n = c0 + c1;
+    }
+    __device__ __forceinline__ int slot(int m) const { return m < 2 * cm ? (m & 1) : tl; }
+    __device__ __forceinline__ int step(int m) const { return m < 2 * cm ? j0 + (m >> 1) : j0 + m - cm; }
+    // op of slot t's step j
+    __device__ __forceinline__ int op(int t, int j) const { return j - j0 < cm ? 2 * (j - j0) + t : j - j0 + cm; }
+    __device__ __forceinline__ bool first_of_step(int m) const { return m >= 2 * cm || !(m & 1); }
+    __device__ __forceinline__ bool last_of_step(int m) const { return m >= 2 * cm || (m & 1); }
+};
 
 // The r-th work unit of this CTA; every role of the CTA walks the same list.
 //
@@ -399,11 +451,12 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
     const int wq = (threadIdx.x >> 5) & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_base + C::col_s(t);
     const uint32_t tO = tmem + lane_base + C::col_o(t);
-    const uint32_t tP = tmem + lane_base + C::col_p(t);
     const float sl2 = p.scale_log2;
-    uint32_t ph_s = 0, ph_te = 0, ph_o = 0;
+    // ph_s: phase bit of step barrier i at bit i; sb: the step barrier this
+    // slot takes next (kRot: in turn over kSBufs, else always 0); pvd: kRot's
+    // P*V-done waits so far (two barriers in turn)
+    uint32_t ph_s = 0, ph_te = 0, ph_o = 0, sb = 0, pvd = 0;
     FA_TRACE_DECL;
     const bool tr = (threadIdx.x & 127) == 0;
 
@@ -427,10 +480,27 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
         // within 2^-6 (without dl the stress workload's worst row measured
         // 1.1e-3 off).  fp16 inputs round O to 2^-11 relative: dl stays 0.
         float dl = 0.f;
+        const OpMap om(un);
         for (int j = un.j0; j < nkv; ++j) {
             const int kt = kKP ? un.kt0 + 2 * j + t : j;   // the key tile in S_t
-            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarSFull + t), ph_s, kSiteSoftmax | (kBarSFull + t))) return;
-            ph_s ^= 1u;
+            // this step's scores (then its P): slot t's own columns, or (kRot)
+            // the buffer of the step's op
+            const uint32_t tS = tmem + lane_base +
+                                (C::kRot ? C::col_sb((uint32_t)om.op(t, j) % (uint32_t)C::kSBufs) : C::col_s(t));
+            const uint32_t tP = tS;
+            const uint32_t bstep = (uint32_t)(kStepBars * t) + sb;
+            if (!ptx::mbar_wait_warp(wc, bars + kBarStride * (kBarSFull + bstep), (ph_s >> sb) & 1u, kSiteSoftmax | (kBarSFull + bstep)))
+                return;
+            ph_s ^= 1u << sb;
+            if constexpr (C::kRot) sb = sb + 1u == (uint32_t)C::kSBufs ? 0u : sb + 1u;
+            // kRot: the slot's previous P*V may still run; it must finish
+            // before O is rescaled, and its barrier is consumed once per step
+            auto pv_done_wait = [&]() -> bool {
+                const uint32_t b = kBarPVDone + 2 * t + (pvd & 1u);
+                const bool ok = ptx::mbar_wait_warp(wc, bars + kBarStride * b, (pvd >> 1) & 1u, kSiteSoftmax | b);
+                ++pvd;
+                return ok;
+            };
             FA_TRACE_EV(tr, t, kEvSReady, j);
             ptx::tc_fence_after();
             // scores of the row; each 32-column load also returns its maximum
@@ -497,6 +567,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             }
             FA_TRACE_EV(tr, t, kEvMaxDone, j);
             if (rescale) {
+                if constexpr (C::kRot) {
+                    if (!pv_done_wait()) return;
+                }
                 // this warp's 32 rows of O_t are scaled by 2^(b_old - b_new)
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
@@ -542,11 +615,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
-                    ptx::mbar_arrive(bars + 8 * (c == 1 ? kBarPHalf + t : kBarPFull + t), lane == 0);
+                    ptx::mbar_arrive(bars + kBarStride * ((c == 1 ? kBarPHalf : kBarPFull) + bstep), lane == 0);
                     if (c == 1) FA_TRACE_EV(tr, t, kEvExpDone, j);
                 }
             }
             FA_TRACE_EV(tr, t, kEvPDone, j);
+            if constexpr (C::kRot) {
+                if (j > un.j0 && !rescale && !pv_done_wait()) return;
+            }
             float sa, sb;
             ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), sa, sb);
             l = fmaf(l, h, sa + sb);
@@ -564,7 +640,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
 #endif
         if constexpr (epi_in_softmax<kBF16, kSplit, kKP>()) {
             // this tile's epilogue, here: O_t is final once its last PV completed
-            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarOFull + t), ph_o, kSiteSoftmax | (kBarOFull + t))) return;
+            if (!ptx::mbar_wait_warp(wc, bars + kBarStride * (kBarOFull + t), ph_o, kSiteSoftmax | (kBarOFull + t))) return;
             ph_o ^= 1u;
             ptx::tc_fence_after();
             const int qrow = q_tile * kBM + row;
@@ -596,15 +672,15 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             if (converts_v<kBF16>() && in && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
             ptx::tc_fence_before();
             __syncwarp();
-            ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t), lane == 0);
+            ptx::mbar_arrive(bars + kBarStride * (kBarOEmpty + t), lane == 0);
         } else {
             // hand (l, b) of every row to the epilogue
-            if (!ptx::mbar_wait_warp(wc, bars + 8 * (kBarStEmpty + t), ph_te ^ 1u, kSiteSoftmax | (kBarStEmpty + t)))
+            if (!ptx::mbar_wait_warp(wc, bars + kBarStride * (kBarStEmpty + t), ph_te ^ 1u, kSiteSoftmax | (kBarStEmpty + t)))
                 return;
             ph_te ^= 1u;
             stats[t * kBM + row] = make_float4(l, b, l + dl, 0.f);
             __syncwarp();
-            ptx::mbar_arrive(bars + 8 * (kBarStFull + t), lane == 0);
+            ptx::mbar_arrive(bars + kBarStride * (kBarStFull + t), lane == 0);
         }
     }
 }
@@ -643,12 +719,12 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             if (un.nkv[0] == 0) continue;
             const bool has1 = un.nkv[1] > 0;
             if (wq == 0) {   // the leader's warp waits, all lanes together
-                bool ok = ptx::mbar_wait(wc, bars + 8 * kBarOFull, ph_o & 1u, kSiteEpilogue | kBarOFull) &&
-                          ptx::mbar_wait(wc, bars + 8 * kBarStFull, ph_t & 1u, kSiteEpilogue | kBarStFull);
+                bool ok = ptx::mbar_wait(wc, bars + kBarStride * kBarOFull, ph_o & 1u, kSiteEpilogue | kBarOFull) &&
+                          ptx::mbar_wait(wc, bars + kBarStride * kBarStFull, ph_t & 1u, kSiteEpilogue | kBarStFull);
                 if (has1)
                     ok = ok &&
-                         ptx::mbar_wait(wc, bars + 8 * (kBarOFull + 1), (ph_o >> 1) & 1u, kSiteEpilogue | (kBarOFull + 1)) &&
-                         ptx::mbar_wait(wc, bars + 8 * (kBarStFull + 1), (ph_t >> 1) & 1u, kSiteEpilogue | (kBarStFull + 1));
+                         ptx::mbar_wait(wc, bars + kBarStride * (kBarOFull + 1), (ph_o >> 1) & 1u, kSiteEpilogue | (kBarOFull + 1)) &&
+                         ptx::mbar_wait(wc, bars + kBarStride * (kBarStFull + 1), (ph_t >> 1) & 1u, kSiteEpilogue | (kBarStFull + 1));
                 ok = __all_sync(0xffffffffu, ok);
                 if (leader) go[0] = ok ? 1u : 0u;
             }
@@ -661,8 +737,8 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             const float4 s0 = stats[row];
             const float4 s1 = has1 ? stats[kBM + row] : make_float4(0.f, -INFINITY, 0.f, 0.f);
             __syncwarp();
-            ptx::mbar_arrive(bars + 8 * kBarStEmpty, lane == 0);
-            ptx::mbar_arrive(bars + 8 * (kBarStEmpty + 1), has1 && lane == 0);
+            ptx::mbar_arrive(bars + kBarStride * kBarStEmpty, lane == 0);
+            ptx::mbar_arrive(bars + kBarStride * (kBarStEmpty + 1), has1 && lane == 0);
             const float m = fmaxf(s0.y, s1.y);   // b0 is finite: the unit's first key tile is unmasked for every row
             const float w0 = ptx::ex2(s0.y - m), w1 = has1 ? ptx::ex2(s1.y - m) : 0.f;
             const float lsum = w0 * s0.x + w1 * s1.x;
@@ -702,8 +778,8 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                 p.ws_lse[slot] = row_lse;
                 ptx::tc_fence_before();
                 __syncwarp();
-                ptx::mbar_arrive(bars + 8 * kBarOEmpty, lane == 0);
-                ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1), has1 && lane == 0);
+                ptx::mbar_arrive(bars + kBarStride * kBarOEmpty, lane == 0);
+                ptx::mbar_arrive(bars + kBarStride * (kBarOEmpty + 1), has1 && lane == 0);
                 continue;
             }
             const int qrow = un.q_tile[0] * kBM + row;
@@ -742,8 +818,8 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             }
             ptx::tc_fence_before();
             __syncwarp();
-            ptx::mbar_arrive(bars + 8 * kBarOEmpty, lane == 0);
-            ptx::mbar_arrive(bars + 8 * (kBarOEmpty + 1), has1 && lane == 0);
+            ptx::mbar_arrive(bars + kBarStride * kBarOEmpty, lane == 0);
+            ptx::mbar_arrive(bars + kBarStride * (kBarOEmpty + 1), has1 && lane == 0);
             ptx::fence_proxy_async_shared();
             ptx::named_bar_sync(1, 128);
             if (leader) {
@@ -760,9 +836,9 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             if (un.nkv[t] == 0) continue;
             if (wq == 0) {   // the leader's warp waits, all lanes together
                 const bool ok = __all_sync(0xffffffffu,
-                                           ptx::mbar_wait(wc, bars + 8 * (kBarOFull + t), (ph_o >> t) & 1u,
+                                           ptx::mbar_wait(wc, bars + kBarStride * (kBarOFull + t), (ph_o >> t) & 1u,
                                                           kSiteEpilogue | (kBarOFull + t)) &&
-                                               ptx::mbar_wait(wc, bars + 8 * (kBarStFull + t), (ph_t >> t) & 1u,
+                                               ptx::mbar_wait(wc, bars + kBarStride * (kBarStFull + t), (ph_t >> t) & 1u,
                                                               kSiteEpilogue | (kBarStFull + t)));
                 if (leader) go[0] = ok ? 1u : 0u;
             }
@@ -774,7 +850,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             ptx::tc_fence_after();
             const float4 st = stats[t * kBM + row];
             __syncwarp();
-            ptx::mbar_arrive(bars + 8 * (kBarStEmpty + t), lane == 0);
+            ptx::mbar_arrive(bars + kBarStride * (kBarStEmpty + t), lane == 0);
             const float inv_l = 1.0f / st.z;   // the sum of the P values the MMAs used
             const float row_lse = (st.y + ptx::lg2(st.x)) * kLn2;
             if constexpr (kSplit) {
@@ -800,7 +876,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                 p.ws_lse[slot] = row_lse;
                 ptx::tc_fence_before();
                 __syncwarp();
-                ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t), lane == 0);
+                ptx::mbar_arrive(bars + kBarStride * (kBarOEmpty + t), lane == 0);
                 FA_TRACE_EV(leader, kTrEpilogue, kEvEpiDone, t);
                 continue;
             }
@@ -837,7 +913,7 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
                 if (box == C::kBoxes - 1) {
                     ptx::tc_fence_before();
                     __syncwarp();
-                    ptx::mbar_arrive(bars + 8 * (kBarOEmpty + t), lane == 0);
+                    ptx::mbar_arrive(bars + kBarStride * (kBarOEmpty + t), lane == 0);
                 }
                 ptx::fence_proxy_async_shared();
                 ptx::named_bar_sync(1, 128);
@@ -875,12 +951,12 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (!ok || un.nkv[t] == 0 || (kKP && t == 1)) continue;   // key-parity units: one Q tile
-            if (!ptx::mbar_wait(wc, bars + 8 * (kBarQEmpty + t), ((ph_qe >> t) & 1u) ^ 1u, kSiteLoad | (kBarQEmpty + t))) {
+            if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarQEmpty + t), ((ph_qe >> t) & 1u) ^ 1u, kSiteLoad | (kBarQEmpty + t))) {
                 ok = false;
                 continue;
             }
             ph_qe ^= 1u << t;
-            const uint32_t fb = bars + 8 * (kBarQFull + t);
+            const uint32_t fb = bars + kBarStride * (kBarQFull + t);
             ptx::mbar_arrive_expect_tx(fb, C::kTileBytes, ex);
             const uint32_t dst = smem_base + C::kOffQ + t * C::kTileBytes;
 #pragma unroll
@@ -898,13 +974,13 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
                     // the entry this copy overwrites must be freed: its pair's release
                     const uint32_t pr = C::pair_of(idx - C::kSlots);
                     const uint32_t b = C::kBarKVEmpty + pr % C::kPairs;
-                    if (!ptx::mbar_wait(wc, bars + 8 * b, (pr / C::kPairs) & 1u, kSiteLoad | b)) {
+                    if (!ptx::mbar_wait(wc, bars + kBarStride * b, (pr / C::kPairs) & 1u, kSiteLoad | b)) {
                         ok = false;
                         break;
                     }
                 }
                 ++kv_count;
-                const uint32_t fb = bars + 8 * (kBarKVFull + (C::kFullPairs ? (idx / 2u) % C::kPairs : slot));
+                const uint32_t fb = bars + kBarStride * (kBarKVFull + (C::kFullPairs ? (idx / 2u) % C::kPairs : slot));
                 ptx::mbar_arrive_expect_tx(fb, C::kSlotBytes, ex);
                 const uint32_t dst = smem_base + C::kOffKV + slot * C::kSlotBytes;
                 const CUtensorMap* m = kind ? tm_v : tm_k;
@@ -923,21 +999,21 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
 #pragma unroll
     for (int t = 0; t < 2; ++t)
         if ((q_issued >> t) & 1u)
-            ptx::mbar_wait_drain(wc, bars + 8 * (kBarQFull + t), ((ph_qe >> t) & 1u) ^ 1u, kSiteDrain | (kBarQFull + t));
+            ptx::mbar_wait_drain(wc, bars + kBarStride * (kBarQFull + t), ((ph_qe >> t) & 1u) ^ 1u, kSiteDrain | (kBarQFull + t));
     if (!C::kFullPairs) {
         for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < kv_count; ++s) {
             const uint32_t last = kv_count - 1 - ((kv_count - 1 - s) % C::kSlots);   // last use of slot s
-            ptx::mbar_wait_drain(wc, bars + 8 * (kBarKVFull + s), (last / C::kSlots) & 1u,
+            ptx::mbar_wait_drain(wc, bars + kBarStride * (kBarKVFull + s), (last / C::kSlots) & 1u,
                                  kSiteDrain | (kBarKVFull + s));
         }
     } else if (kv_count > 0) {
         const uint32_t qmax = (kv_count - 1) / 2;   // the last pair with a copy issued
         // a pair left with only its K copy (an abort in between) gets its
         // second arrival here, so its phase completes once that copy lands
-        if (kv_count & 1u) ptx::mbar_arrive(bars + 8 * (kBarKVFull + qmax % C::kPairs), ex);
+        if (kv_count & 1u) ptx::mbar_arrive(bars + kBarStride * (kBarKVFull + qmax % C::kPairs), ex);
         for (uint32_t b = 0; b < (uint32_t)C::kPairs && b <= qmax; ++b) {
             const uint32_t q = qmax - ((qmax - b) % C::kPairs);   // last pair on barrier b
-            ptx::mbar_wait_drain(wc, bars + 8 * (kBarKVFull + b), (q / C::kPairs) & 1u, kSiteDrain | (kBarKVFull + b));
+            ptx::mbar_wait_drain(wc, bars + kBarStride * (kBarKVFull + b), (q / C::kPairs) & 1u, kSiteDrain | (kBarKVFull + b));
         }
     }
 }
@@ -968,10 +1044,10 @@ __device__ __forceinline__ void vconvert_role(const Params& p, const ptx::WaitCt
             bool ok;
             if constexpr (C::kFullPairs) {
                 const uint32_t q = iv / 2u, b = kBarKVFull + q % C::kPairs;
-                ok = ptx::mbar_wait_warp(wc, bars + 8 * b, (q / C::kPairs) & 1u, kSiteLoad | 0x80u | b);
+                ok = ptx::mbar_wait_warp(wc, bars + kBarStride * b, (q / C::kPairs) & 1u, kSiteLoad | 0x80u | b);
             } else {
                 const uint32_t slot = iv % C::kSlots;
-                ok = ptx::mbar_wait_warp(wc, bars + 8 * (kBarKVFull + slot), (iv / C::kSlots) & 1u,
+                ok = ptx::mbar_wait_warp(wc, bars + kBarStride * (kBarKVFull + slot), (iv / C::kSlots) & 1u,
                                          kSiteLoad | 0x80u | (kBarKVFull + slot));
             }
             if (!ok) return;
@@ -990,7 +1066,7 @@ __device__ __forceinline__ void vconvert_role(const Params& p, const ptx::WaitCt
             }
             ptx::fence_proxy_async_shared();
             __syncwarp();
-            ptx::mbar_arrive(bars + 8 * (C::kBarVConv + iv % C::kSlots), lane == 0);
+            ptx::mbar_arrive(bars + kBarStride * (C::kBarVConv + iv % C::kSlots), lane == 0);
         }
     }
 }
@@ -1014,10 +1090,10 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     auto kv_wait = [&](uint32_t idx) -> bool {
         if constexpr (C::kFullPairs) {
             const uint32_t q = idx / 2u, b = kBarKVFull + q % C::kPairs;
-            return ptx::mbar_wait(wc, bars + 8 * b, (q / C::kPairs) & 1u, kSiteMma | b);
+            return ptx::mbar_wait(wc, bars + kBarStride * b, (q / C::kPairs) & 1u, kSiteMma | b);
         } else {
             const uint32_t slot = idx % C::kSlots;
-            return ptx::mbar_wait(wc, bars + 8 * (kBarKVFull + slot), (idx / C::kSlots) & 1u,
+            return ptx::mbar_wait(wc, bars + kBarStride * (kBarKVFull + slot), (idx / C::kSlots) & 1u,
                                   kSiteMma | (kBarKVFull + slot));
         }
     };
@@ -1025,14 +1101,14 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     auto v_wait = [&](uint32_t idx) -> bool {
         if constexpr (converts_v<kBF16>()) {
             const uint32_t slot = idx % C::kSlots;
-            return ptx::mbar_wait(wc, bars + 8 * (C::kBarVConv + slot), (idx / C::kSlots) & 1u,
+            return ptx::mbar_wait(wc, bars + kBarStride * (C::kBarVConv + slot), (idx / C::kSlots) & 1u,
                                   kSiteMma | (C::kBarVConv + slot));
         } else {
             return kv_wait(idx);
         }
     };
     // frees the pair of ring entries ending at `idx` (see Cfg): one commit
-    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + 8 * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs), ex); };
+    auto kv_release = [&](uint32_t idx) { ptx::mma_commit(bars + kBarStride * (C::kBarKVEmpty + C::pair_of(idx) % C::kPairs), ex); };
     // S_t = Q_t K^T: M = 128 rows, N = 128 keys, K = D in steps of 16 (32 bytes
     // inside a 128-byte swizzled row; the next 64 columns sit in the next box).
     // Descriptors are built once per tile and stepped by adding the offset to
@@ -1040,7 +1116,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     // instructions per MMA are part of what keeps the tensor pipe fed
     // (measured: +4.5% against rebuilding each descriptor).
     constexpr uint32_t kDescHi = ptx::sdesc_hi_sw128(1024);
-    auto issue_qk = [&](int t, uint32_t idx) {
+    auto issue_qk = [&](int t, uint32_t idx, uint32_t scol) {
         // key-parity units: one Q tile; slot t's key tile is the entry's t-th half
         const uint32_t qa = ptx::sdesc_lo(smem_base + C::kOffQ + (kKP ? 0 : t) * C::kTileBytes, 16);
         const uint32_t kb = ptx::sdesc_lo(
@@ -1048,7 +1124,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            ptx::mma_ss(tmem + C::col_s(t), ptx::sdesc_join(qa + off, kDescHi), ptx::sdesc_join(kb + off, kDescHi),
+            ptx::mma_ss(tmem + scol, ptx::sdesc_join(qa + off, kDescHi), ptx::sdesc_join(kb + off, kDescHi),
                         kIdescQK, kk > 0 ? 1u : 0u, ex);
         }
     };
@@ -1056,18 +1132,111 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     // [128 keys x D], D contiguous: 8-key groups 1024 bytes apart, 64-column
     // boxes kBoxBytes apart.
     // One half: keys 64*half .. 64*half+63 (four K=16 steps).
-    auto issue_pv = [&](int t, uint32_t idx, int half, bool acc) {
+    auto issue_pv = [&](int t, uint32_t idx, int half, bool acc, uint32_t pcol) {
         const uint32_t vb = smem_base + C::kOffKV + (idx % C::kSlots) * C::kSlotBytes + (kKP ? t * C::kTileBytes : 0);
         const uint32_t vl = ptx::sdesc_lo(vb, C::kBoxBytes);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = half * 4 + k4;
-            ptx::mma_ts(tmem + C::col_o(t), tmem + C::col_p(t) + kk * 8,
+            ptx::mma_ts(tmem + C::col_o(t), tmem + pcol + kk * 8,
                         ptx::sdesc_join(vl + ((kk * 16 * 128) >> 4), kDescHi), kIdescPV, (acc || kk > 0) ? 1u : 0u, ex);
         }
     };
 
-    for (int r = 0;; ++r) {
+    if constexpr (C::kRot) {
+        // Three score buffers: op m's QK writes buffer m % 3 and the QK of op
+        // m + 3 follows the PV of op m (Cfg::kRot).  Per-slot state in bit
+        // fields, since the slot of an op is a run-time value: qb / pb, 2 bits
+        // per slot, the step barrier its next QK commits to / its next P wait
+        // reads; pph, the phase bit of P barrier 3t + i at that bit; pvn, bit
+        // t, which of slot t's two P*V-done barriers comes next.
+        uint32_t qb = 0u, pb = 0u, pph = 0u, pvn = 0u;
+        auto next3 = [](uint32_t f, int t) {
+            const uint32_t i = (f >> (2 * t)) & 3u;
+            return (f & ~(3u << (2 * t))) | ((i == 2u ? 0u : i + 1u) << (2 * t));
+        };
+        for (int r = 0;; ++r) {
+            const Unit un = unit_at<kSplit, kKP>(r, p);
+            if (un.status == kUnitDone) break;
+            if (un.status == kUnitSkip) continue;
+            const OpMap om(un);
+            if (om.n == 0) continue;
+            // K_j is entry kvb + 2(j - j0) of the ring, V_j the entry after it
+            const uint32_t kvb = kv_count;
+            FA_TRACE_EV(ex != 0u, kTrMma, kEvUnit, un.id);
+            int k_in = un.j0 - 1;   // the last step whose K has been waited for
+            // the QK of op m: slot t's step j into buffer m % 3
+            auto qk_op = [&](int m) -> bool {
+                const int t = om.slot(m), j = om.step(m);
+                if (j == un.j0 && (!kKP || t == 0)) {
+                    // key-parity units: both slots read slot 0's Q buffer
+                    if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarQFull + t), (ph_q >> t) & 1u, kSiteMma | (kBarQFull + t)))
+                        return false;
+                    ph_q ^= 1u << t;
+                }
+                const uint32_t ik = kvb + 2u * (uint32_t)(j - un.j0);
+                if (j > k_in) {
+                    if (!kv_wait(ik)) return false;
+                    k_in = j;
+                }
+                ptx::tc_fence_after();
+                FA_TRACE_EV(ex != 0u, kTrMma, kEvQKGo, ((uint32_t)t << 12) | j);
+                issue_qk(t, ik, C::col_sb((uint32_t)m % 3u));
+                const uint32_t b = kBarSFull + kStepBars * t + ((qb >> (2 * t)) & 3u);
+                ptx::mma_commit(bars + kBarStride * b, ex);
+                qb = next3(qb, t);
+                FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, ((uint32_t)t << 12) | j);
+                // Q is free after its last QK: the unit's last op (key-parity
+                // units), else slot t's last step
+                if (kKP ? m == om.n - 1 : j == (t ? un.nkv[1] : un.nkv[0]) - 1)
+                    ptx::mma_commit(bars + kBarStride * (kBarQEmpty + (kKP ? 0 : t)), ex);
+                return true;
+            };
+            for (int m = 0; m < om.n && m < 3; ++m)
+                if (!qk_op(m)) goto done;
+            kv_release(kvb);
+            for (int m = 0; m < om.n; ++m) {
+                const int t = om.slot(m), j = om.step(m);
+                const uint32_t bi = (uint32_t)(kStepBars * t) + ((pb >> (2 * t)) & 3u);
+                const uint32_t pcol = C::col_sb((uint32_t)m % 3u);
+                const uint32_t iv = kvb + 2u * (uint32_t)(j - un.j0) + 1u;
+                FA_TRACE_EV(ex != 0u, kTrMma, kEvPWait, ((uint32_t)t << 12) | j);
+                if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPHalf + bi), (pph >> bi) & 1u, kSiteMma | (kBarPHalf + bi)))
+                    goto done;
+                if (j == un.j0) {
+                    // O_t is overwritten: the previous unit's epilogue must have read it
+                    if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarOEmpty + t), ((ph_oe >> t) & 1u) ^ 1u,
+                                        kSiteMma | (kBarOEmpty + t)))
+                        goto done;
+                    ph_oe ^= 1u << t;
+                }
+                // V_j, before the step's first P*V (at D=64 with fp16 inputs
+                // the wait for K_j covered it)
+                if (!(C::kFullPairs && !converts_v<kBF16>()) && om.first_of_step(m) && !v_wait(iv)) goto done;
+                ptx::tc_fence_after();
+                FA_TRACE_EV(ex != 0u, kTrMma, kEvPVGo, ((uint32_t)t << 12) | j);
+                issue_pv(t, iv, 0, j > un.j0, pcol);
+                FA_TRACE_EV(ex != 0u, kTrMma, kEvPVMid, ((uint32_t)t << 12) | j);
+                if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPFull + bi), (pph >> bi) & 1u, kSiteMma | (kBarPFull + bi)))
+                    goto done;
+                pph ^= 1u << bi;
+                pb = next3(pb, t);
+                ptx::tc_fence_after();
+                issue_pv(t, iv, 1, true, pcol);
+                FA_TRACE_EV(ex != 0u, kTrMma, kEvPV, ((uint32_t)t << 12) | j);
+                if (j == (t ? un.nkv[1] : un.nkv[0]) - 1) {
+                    ptx::mma_commit(bars + kBarStride * (kBarOFull + t), ex);
+                } else {
+                    ptx::mma_commit(bars + kBarStride * (kBarPVDone + 2 * t + ((pvn >> t) & 1u)), ex);
+                    pvn ^= 1u << t;
+                }
+                // V_j with K_{j+1}: every QK on K_{j+1} (ops up to m + 2) is issued
+                if (om.last_of_step(m) && j + 1 < un.nmax) kv_release(iv + 1u);
+                if (m + 3 < om.n && !qk_op(m + 3)) goto done;
+            }
+            kv_count = kvb + 2 * (un.nmax - un.j0);
+        }
+    } else for (int r = 0;; ++r) {
         const Unit un = unit_at<kSplit, kKP>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
@@ -1085,7 +1254,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
         for (int t = 0; t < 2; ++t) {
             if (un.nkv[t] == 0) continue;
             if (!kKP || t == 0) {
-                if (!ptx::mbar_wait(wc, bars + 8 * (kBarQFull + t), (ph_q >> t) & 1u, kSiteMma | (kBarQFull + t)))
+                if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarQFull + t), (ph_q >> t) & 1u, kSiteMma | (kBarQFull + t)))
                     goto done;
                 ph_q ^= 1u << t;
             }
@@ -1094,11 +1263,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                 k_in = true;
             }
             ptx::tc_fence_after();
-            issue_qk(t, kvb);
-            ptx::mma_commit(bars + 8 * (kBarSFull + t), ex);
+            issue_qk(t, kvb, C::col_s(t));
+            ptx::mma_commit(bars + kBarStride * (kBarSFull + kStepBars * t), ex);
             FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, (uint32_t)t << 12);
             if (un.nkv[t] == un.j0 + 1 && (!kKP || t == qe_slot))
-                ptx::mma_commit(bars + 8 * (kBarQEmpty + (kKP ? 0 : t)), ex);
+                ptx::mma_commit(bars + kBarStride * (kBarQEmpty + (kKP ? 0 : t)), ex);
         }
         kv_release(kvb);
         for (int j = un.j0; j < un.nmax; ++j) {
@@ -1108,12 +1277,13 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             for (int t = 0; t < 2; ++t) {
                 if (j < un.nkv[t]) {
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvPWait, ((uint32_t)t << 12) | j);
-                    if (!ptx::mbar_wait(wc, bars + 8 * (kBarPHalf + t), (ph_ph >> t) & 1u, kSiteMma | (kBarPHalf + t)))
+                    if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPHalf + kStepBars * t), (ph_ph >> t) & 1u,
+                                        kSiteMma | (kBarPHalf + kStepBars * t)))
                         goto done;
                     ph_ph ^= 1u << t;
                     if (j == un.j0) {
                         // O_t is overwritten: the previous unit's epilogue must have read it
-                        if (!ptx::mbar_wait(wc, bars + 8 * (kBarOEmpty + t), ((ph_oe >> t) & 1u) ^ 1u,
+                        if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarOEmpty + t), ((ph_oe >> t) & 1u) ^ 1u,
                                             kSiteMma | (kBarOEmpty + t)))
                             goto done;
                         ph_oe ^= 1u << t;
@@ -1124,15 +1294,16 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     }
                     ptx::tc_fence_after();
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvPVGo, ((uint32_t)t << 12) | j);
-                    issue_pv(t, iv, 0, j > un.j0);
+                    issue_pv(t, iv, 0, j > un.j0, C::col_p(t));
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvPVMid, ((uint32_t)t << 12) | j);
-                    if (!ptx::mbar_wait(wc, bars + 8 * (kBarPFull + t), (ph_p >> t) & 1u, kSiteMma | (kBarPFull + t)))
+                    if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPFull + kStepBars * t), (ph_p >> t) & 1u,
+                                        kSiteMma | (kBarPFull + kStepBars * t)))
                         goto done;
                     ph_p ^= 1u << t;
                     ptx::tc_fence_after();
-                    issue_pv(t, iv, 1, true);
+                    issue_pv(t, iv, 1, true, C::col_p(t));
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvPV, ((uint32_t)t << 12) | j);
-                    if (j == un.nkv[t] - 1) ptx::mma_commit(bars + 8 * (kBarOFull + t), ex);
+                    if (j == un.nkv[t] - 1) ptx::mma_commit(bars + kBarStride * (kBarOFull + t), ex);
                 }
                 if (j + 1 < un.nkv[t]) {
                     if (!k_ready) {
@@ -1141,11 +1312,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                         ptx::tc_fence_after();
                     }
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
-                    issue_qk(t, ik);
-                    ptx::mma_commit(bars + 8 * (kBarSFull + t), ex);
+                    issue_qk(t, ik, C::col_s(t));
+                    ptx::mma_commit(bars + kBarStride * (kBarSFull + kStepBars * t), ex);
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
                     if (j + 1 == un.nkv[t] - 1 && (!kKP || t == qe_slot))
-                        ptx::mma_commit(bars + 8 * (kBarQEmpty + (kKP ? 0 : t)), ex);
+                        ptx::mma_commit(bars + kBarStride * (kBarQEmpty + (kKP ? 0 : t)), ex);
                 }
             }
             // V_j and K_{j+1} together; a unit's last V goes with the next
@@ -1156,8 +1327,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     }
 done:
     // every MMA must be complete before tensor memory is released
-    ptx::mma_commit(bars + 8 * kBarDrain, ex);
-    ptx::mbar_wait_drain(wc, bars + 8 * kBarDrain, 0u, kSiteDrain | kBarDrain);
+    ptx::mma_commit(bars + kBarStride * kBarDrain, ex);
+    ptx::mbar_wait_drain(wc, bars + kBarStride * kBarDrain, 0u, kSiteDrain | kBarDrain);
 }
 
 // ---------------------------------------------------------------------------------
@@ -1186,21 +1357,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
-            ptx::mbar_init(bars + 8 * (kBarQFull + t), 1);
-            ptx::mbar_init(bars + 8 * (kBarQEmpty + t), 1);
-            ptx::mbar_init(bars + 8 * (kBarSFull + t), 1);
-            ptx::mbar_init(bars + 8 * (kBarPHalf + t), 4);
-            ptx::mbar_init(bars + 8 * (kBarPFull + t), 4);
-            ptx::mbar_init(bars + 8 * (kBarOFull + t), 1);
-            ptx::mbar_init(bars + 8 * (kBarOEmpty + t), 4);
-            ptx::mbar_init(bars + 8 * (kBarStFull + t), 4);
-            ptx::mbar_init(bars + 8 * (kBarStEmpty + t), 4);
+            ptx::mbar_init(bars + kBarStride * (kBarQFull + t), 1);
+            ptx::mbar_init(bars + kBarStride * (kBarQEmpty + t), 1);
+            for (int i = 0; i < kStepBars; ++i) {
+                ptx::mbar_init(bars + kBarStride * (kBarSFull + kStepBars * t + i), 1);
+                ptx::mbar_init(bars + kBarStride * (kBarPHalf + kStepBars * t + i), 4);
+                ptx::mbar_init(bars + kBarStride * (kBarPFull + kStepBars * t + i), 4);
+            }
+            ptx::mbar_init(bars + kBarStride * (kBarPVDone + 2 * t), 1);
+            ptx::mbar_init(bars + kBarStride * (kBarPVDone + 2 * t + 1), 1);
+            ptx::mbar_init(bars + kBarStride * (kBarOFull + t), 1);
+            ptx::mbar_init(bars + kBarStride * (kBarOEmpty + t), 4);
+            ptx::mbar_init(bars + kBarStride * (kBarStFull + t), 4);
+            ptx::mbar_init(bars + kBarStride * (kBarStEmpty + t), 4);
         }
-        ptx::mbar_init(bars + 8 * kBarDrain, 1);
+        ptx::mbar_init(bars + kBarStride * kBarDrain, 1);
         for (int s = 0; s < C::kSlots; ++s) {
-            ptx::mbar_init(bars + 8 * (kBarKVFull + s), C::kFullPairs ? 2 : 1);   // (K_j's and V_j's copies)
-            ptx::mbar_init(bars + 8 * (C::kBarKVEmpty + s), 1);
-            ptx::mbar_init(bars + 8 * (C::kBarVConv + s), conv_warps<kBF16, kSplit, kKP>() > 0 ? conv_warps<kBF16, kSplit, kKP>() : 1);
+            ptx::mbar_init(bars + kBarStride * (kBarKVFull + s), C::kFullPairs ? 2 : 1);   // (K_j's and V_j's copies)
+            ptx::mbar_init(bars + kBarStride * (C::kBarKVEmpty + s), 1);
+            ptx::mbar_init(bars + kBarStride * (C::kBarVConv + s), conv_warps<kBF16, kSplit, kKP>() > 0 ? conv_warps<kBF16, kSplit, kKP>() : 1);
         }
         ctl[1] = 0u;
         ptx::fence_mbar_init();
