@@ -1,0 +1,50 @@
+"""The barrier protocol of the three rotating score buffers (FA_SCORE_ROTATION,
+D=64), checked on a CPU model of the kernel's roles over random unit lists and
+random interleavings (tests/protocol_model.py), plus known mistakes the model
+must catch.  The kernel built with the option is checked against the oracle
+on the GPU (test_score_rotation.py)."""
+import random
+
+import pytest
+
+from protocol_model import ProtocolError, random_units, simulate
+
+
+def _run(n_cases, kp, bf16, mistake=None, seed0=0, **kw):
+    """Failures (exceptions or deadlocks) over n_cases unit lists, 2 schedules each."""
+    bad = 0
+    for c in range(n_cases):
+        units = random_units(random.Random(seed0 + c), kp)
+        for s in range(2):
+            try:
+                ok, _ = simulate(units, kp, bf16, random.Random(1000 * c + s), mistake=mistake, **kw)
+            except ProtocolError:
+                ok = False
+            if not ok:
+                bad += 1
+                break
+    return bad
+
+
+@pytest.mark.parametrize("kp", [False, True])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_rotation_protocol_holds(kp, bf16):
+    # no deadlock, no aliased phase, no stale buffer or ring entry, no O rescale with a P*V outstanding
+    assert _run(120, kp, bf16) == 0
+
+
+@pytest.mark.parametrize("mistake", ["two_step_barriers", "lookahead_too_deep", "no_pv_done_wait", "early_release"])
+def test_model_catches_planted_mistakes(mistake):
+    # two step barriers per slot (phases alias once a slot runs three steps
+    # ahead), the QK of op m + 4 after the P*V of op m (it overwrites a buffer
+    # whose P is still to be read), an O rescale
+    # without the P*V-done wait, a ring pair freed before its last reader
+    assert _run(60, True, False, mistake=mistake) + _run(60, False, True, mistake=mistake) > 0
+
+
+def test_paired_kv_barriers_deadlock_on_the_key_parity_ring():
+    # K and V of a step on one full barrier, with key-parity units' 4 double
+    # slots: the unit's first three QKs need the second step's pair, whose V
+    # has no free slot until those QKs release the first -- why the option
+    # gives key-parity units separate K and V barriers
+    assert _run(60, True, False, full_pairs=True) > 0
