@@ -388,22 +388,22 @@ __device__ __forceinline__ Unit unit_at(int r, const Params& p)
         un.nkv[0] = (count + 1) / 2;
         un.nkv[1] = count / 2;
         un.nmax = un.nkv[0];
-        return un;
-    }
+    } else {
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int qt = qg * p.tpu + t;
-        const bool active = (t < p.tpu) && (qt < p.n_qtiles);
-        const int total = kv_tiles_of(qt, p.n_kv, p.causal);
-        un.q_tile[t] = qt;
-        un.last[t] = total - 1;
-        if constexpr (kSplit) {
-            const int end = min(un.j0 + p.split_chunk, total);
-            un.nkv[t] = (active && end > un.j0) ? end : 0;
-        } else {
-            un.nkv[t] = active ? total : 0;
+        for (int t = 0; t < 2; ++t) {
+            const int qt = qg * p.tpu + t;
+            const bool active = (t < p.tpu) && (qt < p.n_qtiles);
+            const int total = kv_tiles_of(qt, p.n_kv, p.causal);
+            un.q_tile[t] = qt;
+            un.last[t] = total - 1;
+            if constexpr (kSplit) {
+                const int end = min(un.j0 + p.split_chunk, total);
+                un.nkv[t] = (active && end > un.j0) ? end : 0;
+            } else {
+                un.nkv[t] = active ? total : 0;
+            }
+            un.nmax = max(un.nmax, un.nkv[t]);
         }
-        un.nmax = max(un.nmax, un.nkv[t]);
     }
     return un;
 }
@@ -458,7 +458,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
     // P*V-done waits so far (two barriers in turn)
     uint32_t ph_s = 0, ph_te = 0, ph_o = 0, sb = 0, pvd = 0;
     FA_TRACE_DECL;
-    const bool tr = (threadIdx.x & 127) == 0;
+    [[maybe_unused]] const bool tr = (threadIdx.x & 127) == 0;   // the warpgroup's trace events (FA_TRACE builds)
 
     for (int r = 0;; ++r) {
         const Unit un = unit_at<kSplit, kKP>(r, p);
@@ -828,102 +828,103 @@ __device__ __forceinline__ void correction_epilogue_role(const Params& p, const 
             }
             if (converts_v<kBF16>() && qrow < p.S && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
             continue;
-        }
-        // one named barrier carries the leader's wait outcome to all 128
-        // threads, so the warpgroup never splits over an abort
+        } else {
+            // one named barrier carries the leader's wait outcome to all 128
+            // threads, so the warpgroup never splits over an abort
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (un.nkv[t] == 0) continue;
-            if (wq == 0) {   // the leader's warp waits, all lanes together
-                const bool ok = __all_sync(0xffffffffu,
-                                           ptx::mbar_wait(wc, bars + kBarStride * (kBarOFull + t), (ph_o >> t) & 1u,
-                                                          kSiteEpilogue | (kBarOFull + t)) &&
-                                               ptx::mbar_wait(wc, bars + kBarStride * (kBarStFull + t), (ph_t >> t) & 1u,
-                                                              kSiteEpilogue | (kBarStFull + t)));
-                if (leader) go[0] = ok ? 1u : 0u;
-            }
-            ptx::named_bar_sync(1, 128);
-            if (go[0] == 0u) goto done;
-            ph_o ^= 1u << t;
-            ph_t ^= 1u << t;
-            FA_TRACE_EV(leader, kTrEpilogue, kEvOFull, t);
-            ptx::tc_fence_after();
-            const float4 st = stats[t * kBM + row];
-            __syncwarp();
-            ptx::mbar_arrive(bars + kBarStride * (kBarStEmpty + t), lane == 0);
-            const float inv_l = 1.0f / st.z;   // the sum of the P values the MMAs used
-            const float row_lse = (st.y + ptx::lg2(st.x)) * kLn2;
-            if constexpr (kSplit) {
-                // split-KV partial: this chunk's O (normalised by its own row
-                // sum) and LSE, fp32, into the workspace slot of the unit
-                const size_t slot = ((size_t)un.id * p.tpu + t) * kBM + row;
-                float* dst = p.ws_o + slot * D;
-                const uint32_t tO = tmem + lane_base + C::col_o(t);
-                float osum = 0.f;   // converted V: a value beyond fp16's range makes O (and this sum) not finite
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32_wait(tO + c0, o);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 x = make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
-                                                     __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
-                        if constexpr (converts_v<kBF16>()) osum += (fabsf(x.x) + fabsf(x.y)) + (fabsf(x.z) + fabsf(x.w));
-                        *reinterpret_cast<float4*>(dst + c0 + i) = x;
-                    }
+            for (int t = 0; t < 2; ++t) {
+                if (un.nkv[t] == 0) continue;
+                if (wq == 0) {   // the leader's warp waits, all lanes together
+                    const bool ok = __all_sync(0xffffffffu,
+                                               ptx::mbar_wait(wc, bars + kBarStride * (kBarOFull + t), (ph_o >> t) & 1u,
+                                                              kSiteEpilogue | (kBarOFull + t)) &&
+                                                   ptx::mbar_wait(wc, bars + kBarStride * (kBarStFull + t), (ph_t >> t) & 1u,
+                                                                  kSiteEpilogue | (kBarStFull + t)));
+                    if (leader) go[0] = ok ? 1u : 0u;
                 }
-                if (converts_v<kBF16>() && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
-                p.ws_lse[slot] = row_lse;
-                ptx::tc_fence_before();
-                __syncwarp();
-                ptx::mbar_arrive(bars + kBarStride * (kBarOEmpty + t), lane == 0);
-                FA_TRACE_EV(leader, kTrEpilogue, kEvEpiDone, t);
-                continue;
-            }
-            const int qrow = un.q_tile[t] * kBM + row;
-            if (qrow < p.S) p.lse[(size_t)un.bh * (size_t)p.S + (size_t)qrow] = row_lse;
-            const uint32_t tO = tmem + lane_base + C::col_o(t);
-            float osum = 0.f;   // converted V: a value beyond fp16's range makes O (and this sum) not finite
-#pragma unroll 1
-            for (int box = 0; box < C::kBoxes; ++box) {
-                // the staging box is free once the previous TMA store has read it
-                if (leader) ptx::bulk_wait_read0();
                 ptx::named_bar_sync(1, 128);
+                if (go[0] == 0u) goto done;
+                ph_o ^= 1u << t;
+                ph_t ^= 1u << t;
+                FA_TRACE_EV(leader, kTrEpilogue, kEvOFull, t);
+                ptx::tc_fence_after();
+                const float4 st = stats[t * kBM + row];
+                __syncwarp();
+                ptx::mbar_arrive(bars + kBarStride * (kBarStEmpty + t), lane == 0);
+                const float inv_l = 1.0f / st.z;   // the sum of the P values the MMAs used
+                const float row_lse = (st.y + ptx::lg2(st.x)) * kLn2;
+                if constexpr (kSplit) {
+                    // split-KV partial: this chunk's O (normalised by its own row
+                    // sum) and LSE, fp32, into the workspace slot of the unit
+                    const size_t slot = ((size_t)un.id * p.tpu + t) * kBM + row;
+                    float* dst = p.ws_o + slot * D;
+                    const uint32_t tO = tmem + lane_base + C::col_o(t);
+                    float osum = 0.f;   // converted V: a value beyond fp16's range makes O (and this sum) not finite
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32_wait(tO + c0, o);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32_wait(tO + box * 64 + half * 32, o);
-                    uint32_t pk[16];
-                    const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float a, b2;
-                        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
-                                       a, b2);
-                        if constexpr (converts_v<kBF16>()) osum += fabsf(a) + fabsf(b2);
-                        pk[i] = ptx::pack2<kBF16>(a, b2);
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 x = make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
+                                                         __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                            if constexpr (converts_v<kBF16>()) osum += (fabsf(x.x) + fabsf(x.y)) + (fabsf(x.z) + fabsf(x.w));
+                            *reinterpret_cast<float4*>(dst + c0 + i) = x;
+                        }
                     }
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int chunk = half * 4 + cc;   // 16-byte chunk of the 128-byte row
-                        const uint32_t addr = stage + row * 128 + ((chunk ^ (row & 7)) << 4);
-                        ptx::st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                    }
-                }
-                if (box == C::kBoxes - 1) {
+                    if (converts_v<kBF16>() && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
+                    p.ws_lse[slot] = row_lse;
                     ptx::tc_fence_before();
                     __syncwarp();
                     ptx::mbar_arrive(bars + kBarStride * (kBarOEmpty + t), lane == 0);
+                    FA_TRACE_EV(leader, kTrEpilogue, kEvEpiDone, t);
+                    continue;
                 }
-                ptx::fence_proxy_async_shared();
-                ptx::named_bar_sync(1, 128);
-                if (leader) {
-                    ptx::tma_store_3d(tm_o, stage, box * 64, un.q_tile[t] * kBM, un.bh);
-                    ptx::bulk_commit();
+                const int qrow = un.q_tile[t] * kBM + row;
+                if (qrow < p.S) p.lse[(size_t)un.bh * (size_t)p.S + (size_t)qrow] = row_lse;
+                const uint32_t tO = tmem + lane_base + C::col_o(t);
+                float osum = 0.f;   // converted V: a value beyond fp16's range makes O (and this sum) not finite
+#pragma unroll 1
+                for (int box = 0; box < C::kBoxes; ++box) {
+                    // the staging box is free once the previous TMA store has read it
+                    if (leader) ptx::bulk_wait_read0();
+                    ptx::named_bar_sync(1, 128);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32_wait(tO + box * 64 + half * 32, o);
+                        uint32_t pk[16];
+                        const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float a, b2;
+                            ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
+                                           a, b2);
+                            if constexpr (converts_v<kBF16>()) osum += fabsf(a) + fabsf(b2);
+                            pk[i] = ptx::pack2<kBF16>(a, b2);
+                        }
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const int chunk = half * 4 + cc;   // 16-byte chunk of the 128-byte row
+                            const uint32_t addr = stage + row * 128 + ((chunk ^ (row & 7)) << 4);
+                            ptx::st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                        }
+                    }
+                    if (box == C::kBoxes - 1) {
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        ptx::mbar_arrive(bars + kBarStride * (kBarOEmpty + t), lane == 0);
+                    }
+                    ptx::fence_proxy_async_shared();
+                    ptx::named_bar_sync(1, 128);
+                    if (leader) {
+                        ptx::tma_store_3d(tm_o, stage, box * 64, un.q_tile[t] * kBM, un.bh);
+                        ptx::bulk_commit();
+                    }
                 }
+                if (converts_v<kBF16>() && qrow < p.S && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
+                FA_TRACE_EV(leader, kTrEpilogue, kEvEpiDone, t);
             }
-            if (converts_v<kBF16>() && qrow < p.S && !(osum <= 3.0e38f)) atomicCAS(p.status, 0u, kSiteRangeV);
-            FA_TRACE_EV(leader, kTrEpilogue, kEvEpiDone, t);
         }
     }
 done:
