@@ -41,22 +41,23 @@ def is_stale(lib: str = LIB) -> bool:
 
 
 def variant_lib(trace: bool = False, exp2_poly_pairs: int = 0, epilogue_in_softmax: bool = False,
-                debug_stats: bool = False, score_rotation: bool = False) -> str:
+                debug_stats: bool = False, score_rotation: bool = False, pv_split: bool = False) -> str:
     """Path of the library built with these options."""
     if debug_stats:
         return os.path.join(PKG, "libfa_fwd_dbg.so")
-    if exp2_poly_pairs or epilogue_in_softmax or score_rotation:
+    if exp2_poly_pairs or epilogue_in_softmax or score_rotation or pv_split:
         tag = (f"poly{exp2_poly_pairs}" if exp2_poly_pairs else "") + ("epism" if epilogue_in_softmax else "") + \
-            ("rot" if score_rotation else "")
+            ("rot" if score_rotation else "") + ("pvsplit" if pv_split else "")
         return os.path.join(PKG, f"libfa_fwd_{tag}.so")
     return TRACE_LIB if trace else LIB
 
 
 def _compile(src: str, ptxas_verbose: bool, trace: bool = False, exp2_poly_pairs: int = 0,
              epilogue_in_softmax: bool = False, debug_stats: bool = False,
-             score_rotation: bool = False) -> tuple[str, str]:
+             score_rotation: bool = False, pv_split: bool = False) -> tuple[str, str]:
     tag = (".trace" if trace else "") + (f".poly{exp2_poly_pairs}" if exp2_poly_pairs else "") + \
-        (".epism" if epilogue_in_softmax else "") + (".dbg" if debug_stats else "") + (".rot" if score_rotation else "")
+        (".epism" if epilogue_in_softmax else "") + (".dbg" if debug_stats else "") + \
+        (".rot" if score_rotation else "") + (".pvsplit" if pv_split else "")
     obj = os.path.join(OBJDIR, os.path.basename(src) + tag + ".o")
     cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj] + (["-DFA_TRACE"] if trace else [])
     if debug_stats:
@@ -67,6 +68,8 @@ def _compile(src: str, ptxas_verbose: bool, trace: bool = False, exp2_poly_pairs
         cmd.append("-DFA_EPILOGUE_IN_SOFTMAX=1")
     if score_rotation:
         cmd.append("-DFA_SCORE_ROTATION=1")
+    if pv_split:
+        cmd.append("-DFA_PV_SPLIT=1")
     if ptxas_verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -77,7 +80,7 @@ def _compile(src: str, ptxas_verbose: bool, trace: bool = False, exp2_poly_pairs
 
 def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None,
           trace: bool = False, exp2_poly_pairs: int = 0, epilogue_in_softmax: bool = False,
-          debug_stats: bool = False, score_rotation: bool = False) -> str:
+          debug_stats: bool = False, score_rotation: bool = False, pv_split: bool = False) -> str:
     """Compile every CUDA translation unit and link libfa_fwd.so (or, with
     trace=True, the event-tracing variant libfa_fwd_trace.so; with
     exp2_poly_pairs=N in 1..16, libfa_fwd_polyN.so, whose softmax computes N of
@@ -85,17 +88,18 @@ def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = N
     libfa_fwd_epism.so, whose softmax warpgroups also run the epilogue; with
     debug_stats, libfa_fwd_dbg.so, which writes each row's final base and sum
     and counts its re-bases; with score_rotation, libfa_fwd_rot.so, whose D=64
-    kernels rotate three score buffers); returns its path."""
+    kernels rotate three score buffers; with pv_split, libfa_fwd_pvsplit.so,
+    whose softmax publishes P in two halves); returns its path."""
     if not 0 <= exp2_poly_pairs <= 16:
         raise ValueError("exp2_poly_pairs must be in [0, 16]")
-    lib = variant_lib(trace, exp2_poly_pairs, epilogue_in_softmax, debug_stats, score_rotation)
+    lib = variant_lib(trace, exp2_poly_pairs, epilogue_in_softmax, debug_stats, score_rotation, pv_split)
     if not force and not ptxas_verbose and not is_stale(lib):
         return lib
     os.makedirs(OBJDIR, exist_ok=True)
     srcs = sources()
     with ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
         results = list(ex.map(lambda s: _compile(s, ptxas_verbose, trace, exp2_poly_pairs, epilogue_in_softmax,
-                                                 debug_stats, score_rotation), srcs))
+                                                 debug_stats, score_rotation, pv_split), srcs))
     if ptxas_verbose:
         for _, log in results:
             if log.strip():

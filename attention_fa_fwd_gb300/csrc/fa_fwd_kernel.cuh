@@ -32,10 +32,10 @@
 //   PV0(j), QK0(j+1), PV1(j), QK1(j+1)
 // so the tensor core computes one tile's scores while the other tile's softmax
 // runs (the FA_SCORE_ROTATION build option issues QK(j+1) earlier still at
-// D=64, into a third score buffer; see Cfg::kRot).  Each PV is issued in two
-// halves (keys 0-63, then 64-127): the softmax
-// publishes the first half of P before it computes the second ("G6", V43, PV
-// split), so half of P*V overlaps the second half of the exponentials.
+// D=64, into a third score buffer; see Cfg::kRot).  The softmax publishes P
+// once it is complete and the issuer sends the tile's P*V after that one wait
+// (the FA_PV_SPLIT build option publishes it in two halves instead, "G6",
+// V43).
 //
 // Softmax uses the conditional rescale of "G6", V41, in the base-2 domain: the
 // row base b only moves when the tile maximum exceeds b + T, so p = 2^(x - b)
@@ -128,6 +128,17 @@ template <bool kBF16, bool kSplit, bool kKP>
 __host__ __device__ constexpr bool epi_in_softmax() { return kEpilogueInSoftmax && !kSplit && !kKP; }
 template <bool kBF16, bool kSplit, bool kKP>
 __host__ __device__ constexpr int conv_warps() { return converts_v<kBF16>() ? (epi_in_softmax<kBF16, kSplit, kKP>() ? 6 : 2) : 0; }
+// P published in two halves (keys 0-63, then 64-127), the first P*V half
+// issued after the first ("G6", V43's PV split, so that half of P*V overlaps
+// the second half of the exponentials).  Off by default: the MMA issuer's
+// extra wait and fence per slot and step cost more than the overlap gains
+// (train 1328-1337 against 1373-1376 TFLOPS, wide 853 against 873-875,
+// 1x1x16384x64 401 against 415; the build option exists to measure that).
+#ifndef FA_PV_SPLIT
+#define FA_PV_SPLIT 0
+#endif
+constexpr bool kPVSplit = FA_PV_SPLIT != 0;
+
 // Three rotating score buffers at D=64 (Cfg::kRot): each slot's next scores
 // are computed while its softmax still works on the current ones.  Off by
 // default: the hand-off chain they remove is not what bounds the D=64
@@ -181,8 +192,8 @@ enum : int {
     kBarQFull = 0,      // [2] Q tile t landed (TMA tx)
     kBarQEmpty = 2,     // [2] last QK of tile t finished (commit)
     kBarSFull = 4,      // [2][kStepBars] scores of slot t's step ready (commit)
-    kBarPHalf = 10,     // [2][kStepBars] P keys 0-63 in TMEM, O_t rescaled (4 softmax warps)
-    kBarPFull = 16,     // [2][kStepBars] P keys 64-127 in TMEM (4 softmax warps)
+    kBarPHalf = 10,     // [2][kStepBars] P keys 0-63 in TMEM, O_t rescaled (4 softmax warps; FA_PV_SPLIT)
+    kBarPFull = 16,     // [2][kStepBars] P in TMEM, O_t rescaled (4 softmax warps)
     kBarOFull = 22,     // [2] last PV of tile t finished (commit)
     kBarOEmpty = 24,    // [2] epilogue done reading O_t (4 epilogue warps)
     kBarStFull = 26,    // [2] row statistics of tile t in shared memory (4 softmax warps)
@@ -583,7 +594,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
             }
             // p = 2^(s * scale*log2e - b): one packed FMA per pair, two ex2,
             // packed row sums in four independent accumulators; P is published
-            // in two halves of 64 keys
+            // once complete (with FA_PV_SPLIT also after its first 64 keys)
             const float nb = (b == -INFINITY) ? 0.f : -b;
             const uint64_t c2 = ptx::f2_pack(sl2, sl2), nb2 = ptx::f2_pack(nb, nb);
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -610,8 +621,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                     pk[i] = ptx::pack2<p_is_bf16<kBF16>()>(p0, p1);
                 }
                 ptx::tmem_st16(tP + c * 16, pk);
-                if (c == 1 || c == 3) {
-                    // publish P (and, at c == 1, the rescaled O) for the MMA issuer
+                if ((kPVSplit && c == 1) || c == 3) {
+                    // publish P (and the rescaled O) for the MMA issuer: whole,
+                    // or with FA_PV_SPLIT keys 0-63 at c == 1
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
@@ -1202,8 +1214,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                 const uint32_t pcol = C::col_sb((uint32_t)m % 3u);
                 const uint32_t iv = kvb + 2u * (uint32_t)(j - un.j0) + 1u;
                 FA_TRACE_EV(ex != 0u, kTrMma, kEvPWait, ((uint32_t)t << 12) | j);
-                if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPHalf + bi), (pph >> bi) & 1u, kSiteMma | (kBarPHalf + bi)))
-                    goto done;
+                const uint32_t bp = kPVSplit ? kBarPHalf + bi : kBarPFull + bi;   // the first P wait
+                if (!ptx::mbar_wait(wc, bars + kBarStride * bp, (pph >> bi) & 1u, kSiteMma | bp)) goto done;
                 if (j == un.j0) {
                     // O_t is overwritten: the previous unit's epilogue must have read it
                     if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarOEmpty + t), ((ph_oe >> t) & 1u) ^ 1u,
@@ -1218,11 +1230,13 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                 FA_TRACE_EV(ex != 0u, kTrMma, kEvPVGo, ((uint32_t)t << 12) | j);
                 issue_pv(t, iv, 0, j > un.j0, pcol);
                 FA_TRACE_EV(ex != 0u, kTrMma, kEvPVMid, ((uint32_t)t << 12) | j);
-                if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPFull + bi), (pph >> bi) & 1u, kSiteMma | (kBarPFull + bi)))
-                    goto done;
+                if constexpr (kPVSplit) {
+                    if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPFull + bi), (pph >> bi) & 1u, kSiteMma | (kBarPFull + bi)))
+                        goto done;
+                    ptx::tc_fence_after();
+                }
                 pph ^= 1u << bi;
                 pb = next3(pb, t);
-                ptx::tc_fence_after();
                 issue_pv(t, iv, 1, true, pcol);
                 FA_TRACE_EV(ex != 0u, kTrMma, kEvPV, ((uint32_t)t << 12) | j);
                 if (j == (t ? un.nkv[1] : un.nkv[0]) - 1) {
@@ -1278,9 +1292,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             for (int t = 0; t < 2; ++t) {
                 if (j < un.nkv[t]) {
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvPWait, ((uint32_t)t << 12) | j);
-                    if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPHalf + kStepBars * t), (ph_ph >> t) & 1u,
-                                        kSiteMma | (kBarPHalf + kStepBars * t)))
-                        goto done;
+                    // P_t (with FA_PV_SPLIT: its first half)
+                    const uint32_t bp = (kPVSplit ? kBarPHalf : kBarPFull) + kStepBars * t;
+                    if (!ptx::mbar_wait(wc, bars + kBarStride * bp, (ph_ph >> t) & 1u, kSiteMma | bp)) goto done;
                     ph_ph ^= 1u << t;
                     if (j == un.j0) {
                         // O_t is overwritten: the previous unit's epilogue must have read it
@@ -1297,11 +1311,13 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvPVGo, ((uint32_t)t << 12) | j);
                     issue_pv(t, iv, 0, j > un.j0, C::col_p(t));
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvPVMid, ((uint32_t)t << 12) | j);
-                    if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPFull + kStepBars * t), (ph_p >> t) & 1u,
-                                        kSiteMma | (kBarPFull + kStepBars * t)))
-                        goto done;
-                    ph_p ^= 1u << t;
-                    ptx::tc_fence_after();
+                    if constexpr (kPVSplit) {
+                        if (!ptx::mbar_wait(wc, bars + kBarStride * (kBarPFull + kStepBars * t), (ph_p >> t) & 1u,
+                                            kSiteMma | (kBarPFull + kStepBars * t)))
+                            goto done;
+                        ph_p ^= 1u << t;
+                        ptx::tc_fence_after();
+                    }
                     issue_pv(t, iv, 1, true, C::col_p(t));
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvPV, ((uint32_t)t << 12) | j);
                     if (j == un.nkv[t] - 1) ptx::mma_commit(bars + kBarStride * (kBarOFull + t), ex);

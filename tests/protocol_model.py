@@ -62,9 +62,10 @@ class ProtocolError(AssertionError):
     pass
 
 
-def simulate(units, kp, bf16, rng, mistake=None, full_pairs=None, kslots=None):
+def simulate(units, kp, bf16, rng, mistake=None, full_pairs=None, kslots=None, pv_split=False):
     """units: (j0, nkv0, nkv1) per unit (nkv: end of the slot's steps, 0 =
     absent).  kp: key-parity units (one Q buffer, 4 double ring slots).
+    pv_split: P published in two halves, the issuer waiting for each.
     Returns (True, None), or (False, waits) on deadlock; raises ProtocolError."""
     if full_pairs is None:
         full_pairs = not kp
@@ -202,14 +203,15 @@ def simulate(units, kp, bf16, rng, mistake=None, full_pairs=None, kslots=None):
                 t, j = om.slot(m), om.step(m)
                 bi, iv = pb[t], kvb + 2 * (j - j0) + 1
                 n_ = npw.get((t, bi), 0)
-                yield W(("PHalf", t, bi), (pph >> (3 * t + bi)) & 1, n_)
+                yield W(("PHalf" if pv_split else "PFull", t, bi), (pph >> (3 * t + bi)) & 1, n_)
                 if j == j0:
                     yield W(("OEmpty", t), ((ph_oe >> t) & 1) ^ 1, noe[t] - 1)
                     ph_oe ^= 1 << t
                     noe[t] += 1
                 if not (full_pairs and not bf16) and om.first_of_step(m):
                     yield from v_wait(iv)
-                yield W(("PFull", t, bi), (pph >> (3 * t + bi)) & 1, n_)
+                if pv_split:
+                    yield W(("PFull", t, bi), (pph >> (3 * t + bi)) & 1, n_)
                 npw[(t, bi)] = n_ + 1
                 pph ^= 1 << (3 * t + bi)
                 pb[t] = (bi + 1) % step_bars
@@ -252,7 +254,8 @@ def simulate(units, kp, bf16, rng, mistake=None, full_pairs=None, kslots=None):
                         yield W(("PVDone", t, pvd & 1), (pvd >> 1) & 1, pvd >> 1)
                     pvd += 1
                     check(pv_issued[(ui, t)] == j - j0, "O rescaled while a P*V of the slot is outstanding")
-                B[("PHalf", t, bs)].arrive()
+                if pv_split:
+                    B[("PHalf", t, bs)].arrive()
                 p_arrivals[(ui, m)] = p_arrivals.get((ui, m), 0) + 1
                 if p_arrivals[(ui, m)] == 4:
                     buf[m % 3] = (ui, m, "P")

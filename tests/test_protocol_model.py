@@ -28,9 +28,11 @@ def _run(n_cases, kp, bf16, mistake=None, seed0=0, **kw):
 
 @pytest.mark.parametrize("kp", [False, True])
 @pytest.mark.parametrize("bf16", [False, True])
-def test_rotation_protocol_holds(kp, bf16):
-    # no deadlock, no aliased phase, no stale buffer or ring entry, no O rescale with a P*V outstanding
-    assert _run(120, kp, bf16) == 0
+@pytest.mark.parametrize("pv_split", [False, True])
+def test_rotation_protocol_holds(kp, bf16, pv_split):
+    # no deadlock, no aliased phase, no stale buffer or ring entry, no O
+    # rescale with a P*V outstanding; P published whole or in two halves
+    assert _run(80, kp, bf16, pv_split=pv_split) == 0
 
 
 @pytest.mark.parametrize("mistake", ["two_step_barriers", "lookahead_too_deep", "no_pv_done_wait", "early_release"])
