@@ -263,6 +263,14 @@ struct Cfg {
 
 static_assert(Cfg<64, true>::kSmemBytes <= Cfg<64>::kSmemBytes, "key-parity instances fit the D=64 launch geometry");
 
+// bf16 inputs with K and V on separate full barriers (D=128): the V
+// converters announce V_j only once K_{j+1} has landed too, so the MMA
+// issuer's one wait per key step for the converted V_j also covers the next
+// QKs' K (its own wait for K_{j+1} and the fence after it go: one wait and one
+// fence fewer per step on the issuing thread).  K_{j+1} lands right after V_j.
+template <int D, bool kBF16, bool kKP>
+__host__ __device__ constexpr bool conv_covers_k() { return converts_v<kBF16>() && !Cfg<D, kKP>::kFullPairs && !Cfg<D, kKP>::kRot; }
+
 struct Unit {
     int status;      // kUnitDone, kUnitOk or kUnitSkip
     int id;          // position of the unit in the schedule (split: its workspace slot)
@@ -1079,6 +1087,15 @@ __device__ __forceinline__ void vconvert_role(const Params& p, const ptx::WaitCt
             }
             ptx::fence_proxy_async_shared();
             __syncwarp();
+            if constexpr (conv_covers_k<D, true, kKP>()) {
+                // K_{j+1} (a unit's first K the issuer waits for itself)
+                if (j + 1 < un.nmax) {
+                    const uint32_t ik = iv + 1u, slot = ik % C::kSlots;
+                    if (!ptx::mbar_wait_warp(wc, bars + kBarStride * (kBarKVFull + slot), (ik / C::kSlots) & 1u,
+                                             kSiteLoad | 0x80u | (kBarKVFull + slot)))
+                        return;
+                }
+            }
             ptx::mbar_arrive(bars + kBarStride * (C::kBarVConv + iv % C::kSlots), lane == 0);
         }
     }
@@ -1324,9 +1341,12 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                 }
                 if (j + 1 < un.nkv[t]) {
                     if (!k_ready) {
-                        if (!kv_wait(ik)) goto done;
+                        // (bf16 at D=128: covered by this step's wait for the converted V_j)
+                        if constexpr (!conv_covers_k<D, kBF16, kKP>()) {
+                            if (!kv_wait(ik)) goto done;
+                            ptx::tc_fence_after();
+                        }
                         k_ready = true;
-                        ptx::tc_fence_after();
                     }
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
                     issue_qk(t, ik, C::col_s(t));
