@@ -230,6 +230,10 @@ struct Cfg {
     // (measured 5-9% slower there, 2-3% faster at D=64).  kSlots barriers are
     // reserved per side.
     static constexpr bool kFullPairs = (D == 64) && !(kKP && kScoreRotation);
+    // Two-tile units: the softmax warp that sees a key step's last scores
+    // frees the pair (V_{j-1}, K_j) (that step's last QK comes after the
+    // previous step's every P*V), not a commit from the MMA issuer.
+    static constexpr bool kSoftmaxRelease = (D == 64) && !kKP && !kScoreRotation;
     static constexpr int kPairs = kSlots / 2;
     static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
     __device__ static constexpr uint32_t pair_of(uint32_t entry) { return (entry + 1u) / 2u; }
@@ -479,10 +483,13 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
     FA_TRACE_DECL;
     [[maybe_unused]] const bool tr = (threadIdx.x & 127) == 0;   // the warpgroup's trace events (FA_TRACE builds)
 
+    uint32_t kv_next = 0;   // kSoftmaxRelease: the ring entry of the next unit's first K
     for (int r = 0;; ++r) {
         const Unit un = unit_at<kSplit, kKP>(r, p);
         if (un.status == kUnitDone) break;
         if (un.status == kUnitSkip) continue;
+        const uint32_t kvb = kv_next;   // K_j is ring entry kvb + 2(j - j0)
+        kv_next += 2u * (uint32_t)max(0, un.nmax - un.j0);
         // t is a runtime value: select instead of indexing, so the unit stays in registers
         const int nkv = t ? un.nkv[1] : un.nkv[0];
         const int q_tile = t ? un.q_tile[1] : un.q_tile[0];
@@ -512,6 +519,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                 return;
             ph_s ^= 1u << sb;
             if constexpr (C::kRot) sb = sb + 1u == (uint32_t)C::kSBufs ? 0u : sb + 1u;
+            if constexpr (C::kSoftmaxRelease) {
+                // this step's last QK (slot 1's, or slot 0's when slot 1 is
+                // done or absent) has finished, and with it every P*V of the
+                // step before: V_{j-1} and K_j are free
+                if ((t == 1 || j >= un.nkv[1]) && wq == 0)
+                    ptx::mbar_arrive(bars + kBarStride * (C::kBarKVEmpty + C::pair_of(kvb + 2u * (uint32_t)(j - un.j0)) % C::kPairs),
+                                     lane == 0);
+            }
             // kRot: the slot's previous P*V may still run; it must finish
             // before O is rescaled, and its barrier is consumed once per step
             auto pv_done_wait = [&]() -> bool {
@@ -1301,7 +1316,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             if (un.nkv[t] == un.j0 + 1 && (!kKP || t == qe_slot))
                 ptx::mma_commit(bars + kBarStride * (kBarQEmpty + (kKP ? 0 : t)), ex);
         }
-        kv_release(kvb);
+        if constexpr (!C::kSoftmaxRelease) kv_release(kvb);
         for (int j = un.j0; j < un.nmax; ++j) {
             const uint32_t iv = kvb + 2 * (j - un.j0) + 1, ik = iv + 1;
             bool v_ready = C::kFullPairs && !converts_v<kBF16>(), k_ready = false;
@@ -1358,7 +1373,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             }
             // V_j and K_{j+1} together; a unit's last V goes with the next
             // unit's first K (released after that unit's first QKs)
-            if (j + 1 < un.nmax) kv_release(ik);
+            if (!C::kSoftmaxRelease && j + 1 < un.nmax) kv_release(ik);
         }
         kv_count = kvb + 2 * (un.nmax - un.j0);
     }
