@@ -1,8 +1,10 @@
-"""The barrier protocol of the three rotating score buffers (FA_SCORE_ROTATION,
-D=64), checked on a CPU model of the kernel's roles over random unit lists and
-random interleavings (tests/protocol_model.py), plus known mistakes the model
-must catch.  The kernel built with the option is checked against the oracle
-on the GPU (test_score_rotation.py)."""
+"""The kernel's barrier protocols, checked on a CPU model of its roles over
+random unit lists and random interleavings (tests/protocol_model.py): the
+default order (two-tile units with the ring freed by the softmax at D=64,
+key-parity units, D=128 with the converters covering K) and the three
+rotating score buffers of FA_SCORE_ROTATION, plus known mistakes the model
+must catch.  The kernels themselves are checked against the oracle on the GPU
+(test_parity.py, test_score_rotation.py, ...)."""
 import random
 
 import pytest
@@ -50,3 +52,43 @@ def test_paired_kv_barriers_deadlock_on_the_key_parity_ring():
     # has no free slot until those QKs release the first -- why the option
     # gives key-parity units separate K and V barriers
     assert _run(60, True, False, full_pairs=True) > 0
+
+
+def _run_default(n_cases, kp, bf16, seed0=0, **kw):
+    from protocol_model import simulate_default
+    bad = 0
+    for c in range(n_cases):
+        units = random_units(random.Random(seed0 + c), kp)
+        for s in range(2):
+            try:
+                ok, _ = simulate_default(units, kp, bf16, random.Random(1000 * c + s), **kw)
+            except ProtocolError:
+                ok = False
+            if not ok:
+                bad += 1
+                break
+    return bad
+
+
+@pytest.mark.parametrize("kp,bf16,kw", [
+    (False, False, dict(softmax_release=True)),            # two-tile D=64 (the ring freed by the softmax)
+    (False, True, dict(softmax_release=True)),
+    (True, False, dict()),                                 # key-parity units (issuer commits)
+    (True, True, dict()),
+    (False, True, dict(d128=True, covers_k=True)),         # D=128 bf16 (the converters cover K)
+    (False, False, dict(d128=True)),                       # D=128 fp16
+])
+def test_default_protocol_holds(kp, bf16, kw):
+    assert _run_default(80, kp, bf16, **kw) == 0
+
+
+def test_softmax_release_would_break_key_parity_units():
+    # a key-parity unit's last step can be slot 0's alone while slot 1's last
+    # P*V is still to be issued: slot 0's scores do not cover it, so the ring
+    # keeps the issuer's commit there
+    assert _run_default(80, True, False, softmax_release=True) > 0
+
+
+def test_model_catches_an_uncovered_k():
+    # the issuer skipping its wait for K_{j+1} while the converters do not wait for it either
+    assert _run_default(80, False, True, d128=True, covers_k=True, mistake="converter_skips_k") > 0
