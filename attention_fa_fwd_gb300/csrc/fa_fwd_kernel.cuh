@@ -234,6 +234,13 @@ struct Cfg {
     // frees the pair (V_{j-1}, K_j) (that step's last QK comes after the
     // previous step's every P*V), not a commit from the MMA issuer.
     static constexpr bool kSoftmaxRelease = (D == 64) && !kKP && !kScoreRotation;
+    // Two-tile units at D=128: no release at all.  The loader waits, before
+    // reusing the pair (V_{j-1}, K_j)'s slots, on the score barrier of step
+    // j's last QK itself (that commit completes when the same MMAs do).  Each
+    // slot's score barriers then alternate between two: the loader runs at
+    // most one step behind them, so a parity wait never aliases (the 8-entry
+    // ring at D=64 would let it run three behind).
+    static constexpr bool kLoaderOnScores = (D == 128) && !kKP && !kScoreRotation;
     static constexpr int kPairs = kSlots / 2;
     static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
     __device__ static constexpr uint32_t pair_of(uint32_t entry) { return (entry + 1u) / 2u; }
@@ -515,10 +522,15 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                                 (C::kRot ? C::col_sb((uint32_t)om.op(t, j) % (uint32_t)C::kSBufs) : C::col_s(t));
             const uint32_t tP = tS;
             const uint32_t bstep = (uint32_t)(kStepBars * t) + sb;
+            // the step's P barrier: in turn with the scores' under kRot, else the slot's first
+            const uint32_t bpub = C::kRot ? bstep : (uint32_t)(kStepBars * t);
             if (!ptx::mbar_wait_warp(wc, bars + kBarStride * (kBarSFull + bstep), (ph_s >> sb) & 1u, kSiteSoftmax | (kBarSFull + bstep)))
                 return;
             ph_s ^= 1u << sb;
-            if constexpr (C::kRot) sb = sb + 1u == (uint32_t)C::kSBufs ? 0u : sb + 1u;
+            if constexpr (C::kRot)
+                sb = sb + 1u == (uint32_t)C::kSBufs ? 0u : sb + 1u;
+            else if constexpr (C::kLoaderOnScores)
+                sb ^= 1u;
             if constexpr (C::kSoftmaxRelease) {
                 // this step's last QK (slot 1's, or slot 0's when slot 1 is
                 // done or absent) has finished, and with it every P*V of the
@@ -650,7 +662,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const ptx::WaitCtx
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
-                    ptx::mbar_arrive(bars + kBarStride * ((c == 1 ? kBarPHalf : kBarPFull) + bstep), lane == 0);
+                    ptx::mbar_arrive(bars + kBarStride * ((c == 1 ? kBarPHalf : kBarPFull) + bpub), lane == 0);
                     if (c == 1) FA_TRACE_EV(tr, t, kEvExpDone, j);
                 }
             }
@@ -980,6 +992,11 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
     uint32_t kv_count = 0;
     bool ok = true;
     FA_TRACE_DECL;
+    // kLoaderOnScores: the release of key step g (counted over the CTA's
+    // units) is the score barrier of its last QK: slot s's n-th step, kept as
+    // s << 31 | n for the last two steps (h[g & 1]); cnt0 / cnt1 count each
+    // slot's steps so far, g the steps
+    uint32_t g = 0, cnt0 = 0, cnt1 = 0, h0 = 0, h1 = 0;
     for (int r = 0; ok; ++r) {
         const Unit un = unit_at<kSplit, kKP>(r, p);
         if (un.status == kUnitDone) break;
@@ -1002,11 +1019,23 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
             FA_TRACE_EV(ex != 0u, kTrLoad, kEvQLoad, t);
         }
         for (int j = un.j0; j < un.nmax && ok; ++j) {
+            // two-tile units: slot 1, when present, has every step of the unit
+            const uint32_t last = j < un.nkv[1] ? 1u : 0u;
+            const uint32_t info = (last << 31) | (last ? cnt1 : cnt0);
 #pragma unroll 1
             for (int kind = 0; kind < 2; ++kind) {
                 const uint32_t idx = kv_count;
                 const uint32_t slot = idx % C::kSlots;
-                if (idx >= (uint32_t)C::kSlots) {
+                if (C::kLoaderOnScores && idx >= (uint32_t)C::kSlots) {
+                    // K_j reuses the slots freed by step g - 2, V_j by step g - 1
+                    const uint32_t hs = ((g + (uint32_t)kind) & 1u) ? h1 : h0;
+                    const uint32_t sl = hs >> 31, n = hs & 0x7FFFFFFFu;
+                    const uint32_t b = kBarSFull + kStepBars * sl + (n & 1u);
+                    if (!ptx::mbar_wait(wc, bars + kBarStride * b, (n >> 1) & 1u, kSiteLoad | b)) {
+                        ok = false;
+                        break;
+                    }
+                } else if (idx >= (uint32_t)C::kSlots) {
                     // the entry this copy overwrites must be freed: its pair's release
                     const uint32_t pr = C::pair_of(idx - C::kSlots);
                     const uint32_t b = C::kBarKVEmpty + pr % C::kPairs;
@@ -1014,6 +1043,9 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
                         ok = false;
                         break;
                     }
+                }
+                if (kind == 0) {   // step g - 2's entry is used: step g's takes its place
+                    if (g & 1u) h1 = info; else h0 = info;
                 }
                 ++kv_count;
                 const uint32_t fb = bars + kBarStride * (kBarKVFull + (C::kFullPairs ? (idx / 2u) % C::kPairs : slot));
@@ -1029,6 +1061,9 @@ __device__ __forceinline__ void load_role(const Params& p, const ptx::WaitCtx& w
                     ptx::tma_load_3d(m, dst + bx * C::kBoxBytes, fb, bx * 64, row0, un.bh, ex);
                 FA_TRACE_EV(ex != 0u, kTrLoad, kEvKVLoad, idx);
             }
+            if (j < un.nkv[0]) ++cnt0;
+            if (j < un.nkv[1]) ++cnt1;
+            ++g;
         }
     }
     // Every issued copy must land before the CTA exits (after an abort, too).
@@ -1127,6 +1162,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
     constexpr uint32_t kIdescQK = ptx::idesc_f16(kBM, kBN, kBF16, false);   // Q, K both K-major
     constexpr uint32_t kIdescPV = ptx::idesc_f16(kBM, D, p_is_bf16<kBF16>(), true);   // V MN-major (D contiguous)
     uint32_t ph_q = 0u, ph_ph = 0u, ph_p = 0u, ph_oe = 0u;   // phase bit of tile t at bit t
+    uint32_t sq = 0u;   // kLoaderOnScores: bit t, which of slot t's two score barriers the next QK commits to
     uint32_t kv_count = 0;
     FA_TRACE_DECL;
 
@@ -1311,12 +1347,13 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             }
             ptx::tc_fence_after();
             issue_qk(t, kvb, C::col_s(t));
-            ptx::mma_commit(bars + kBarStride * (kBarSFull + kStepBars * t), ex);
+            ptx::mma_commit(bars + kBarStride * (kBarSFull + kStepBars * t + ((sq >> t) & 1u)), ex);
+            if constexpr (C::kLoaderOnScores) sq ^= 1u << t;
             FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, (uint32_t)t << 12);
             if (un.nkv[t] == un.j0 + 1 && (!kKP || t == qe_slot))
                 ptx::mma_commit(bars + kBarStride * (kBarQEmpty + (kKP ? 0 : t)), ex);
         }
-        if constexpr (!C::kSoftmaxRelease) kv_release(kvb);
+        if constexpr (!C::kSoftmaxRelease && !C::kLoaderOnScores) kv_release(kvb);
         for (int j = un.j0; j < un.nmax; ++j) {
             const uint32_t iv = kvb + 2 * (j - un.j0) + 1, ik = iv + 1;
             bool v_ready = C::kFullPairs && !converts_v<kBF16>(), k_ready = false;
@@ -1365,7 +1402,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
                     }
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvQKGo, ((uint32_t)t << 12) | (j + 1));
                     issue_qk(t, ik, C::col_s(t));
-                    ptx::mma_commit(bars + kBarStride * (kBarSFull + kStepBars * t), ex);
+                    ptx::mma_commit(bars + kBarStride * (kBarSFull + kStepBars * t + ((sq >> t) & 1u)), ex);
+                    if constexpr (C::kLoaderOnScores) sq ^= 1u << t;
                     FA_TRACE_EV(ex != 0u, kTrMma, kEvQK, ((uint32_t)t << 12) | (j + 1));
                     if (j + 1 == un.nkv[t] - 1 && (!kKP || t == qe_slot))
                         ptx::mma_commit(bars + kBarStride * (kBarQEmpty + (kKP ? 0 : t)), ex);
@@ -1373,7 +1411,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const ptx::WaitCtx& wc
             }
             // V_j and K_{j+1} together; a unit's last V goes with the next
             // unit's first K (released after that unit's first QKs)
-            if (!C::kSoftmaxRelease && j + 1 < un.nmax) kv_release(ik);
+            if (!C::kSoftmaxRelease && !C::kLoaderOnScores && j + 1 < un.nmax) kv_release(ik);
         }
         kv_count = kvb + 2 * (un.nmax - un.j0);
     }

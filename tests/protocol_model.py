@@ -75,6 +75,7 @@ def simulate(units, kp, bf16, rng, mistake=None, full_pairs=None, kslots=None, p
     n_slots = kslots or (4 if kp else 8)
     n_pairs = n_slots // 2
     step_bars = 2 if mistake == "two_step_barriers" else 3
+    loader_on_scores, n_sbars = False, 1   # (the loader below is shared in form with simulate_default's)
     look = 4 if mistake == "lookahead_too_deep" else 3
     B = {}
     for t in range(2):
@@ -111,6 +112,7 @@ def simulate(units, kp, bf16, rng, mistake=None, full_pairs=None, kslots=None, p
 
     def loader():
         ph_qe, kvc, nq = 0, 0, [0, 0]
+        g, cnt, hist = 0, [0, 0], [None, None]
         for (j0, n0, n1) in units:
             nkv = (n0, n1)
             for t in range(2):
@@ -120,17 +122,28 @@ def simulate(units, kp, bf16, rng, mistake=None, full_pairs=None, kslots=None, p
                 ph_qe ^= 1 << t
                 nq[t] += 1
                 B[("QFull", t)].arrive()
-            for _ in range(j0, max(n0, n1)):
-                for _kind in range(2):
+            for j in range(j0, max(n0, n1)):
+                last = 1 if j < n1 else 0
+                info = (last, cnt[last])
+                for kind in range(2):
                     idx, s = kvc, kvc % n_slots
                     if idx >= n_slots:
-                        pr = (idx - n_slots + 1) // 2
-                        yield W(("KVEmpty", pr % n_pairs), (pr // n_pairs) & 1, pr // n_pairs)
+                        if loader_on_scores:
+                            sl, n = hist[(g + kind) & 1]
+                            yield W(("SFull", sl, n % n_sbars), (n // n_sbars) & 1, n // n_sbars)
+                        else:
+                            pr = (idx - n_slots + 1) // 2
+                            yield W(("KVEmpty", pr % n_pairs), (pr // n_pairs) & 1, pr // n_pairs)
                         old = slot_entry[s]
                         check(reads_left[old] == 0, f"ring entry {old} overwritten with {reads_left[old]} reads left")
+                    if kind == 0:
+                        hist[g & 1] = info
                     kvc += 1
                     slot_entry[s] = idx
                     B[("KVFull", (idx // 2) % n_pairs if full_pairs else s)].arrive()
+                for t in range(2):
+                    cnt[t] += j < nkv[t]
+                g += 1
 
     def converter():
         kvc = 0
@@ -361,7 +374,8 @@ def random_units(rng, kp):
     return units
 
 
-def simulate_default(units, kp, bf16, rng, d128=False, softmax_release=False, covers_k=False, mistake=None):
+def simulate_default(units, kp, bf16, rng, d128=False, softmax_release=False, covers_k=False, loader_on_scores=False,
+                     mistake=None):
     """The default order (one score buffer per slot): per key step j, slot
     0's P*V then its QK(j+1), then slot 1's; P is published once per step.
     d128: head dim 128 (K and V on separate full barriers, a 4-entry ring;
@@ -371,16 +385,23 @@ def simulate_default(units, kp, bf16, rng, d128=False, softmax_release=False, co
     when slot 1 has no step j), not by an issuer commit.  covers_k (bf16,
     d128): the V converters announce V_j only once K_{j+1} has landed, and the
     issuer's wait for the converted V_j covers the next QKs' K.
-    mistake="converter_skips_k": the issuer relies on covers_k, the
-    converters do not wait for K_{j+1}."""
+    loader_on_scores (d128 two-tile): no ring release at all; before reusing
+    the slots of the pair (V_{g-1}, K_g) the loader waits on the score barrier
+    of key step g's last QK, each slot's score barriers alternating between
+    two.  mistake="converter_skips_k": the issuer relies on covers_k, the
+    converters do not wait for K_{j+1}; mistake="one_score_barrier": the
+    loader waits on scores with one barrier per slot."""
+    n_sbars = 2 if (loader_on_scores and mistake != "one_score_barrier") else 1
     full_pairs = not d128
     n_slots = 4 if (kp or d128) else 8
     n_pairs = n_slots // 2
     B = {}
     for t in range(2):
         for name, c in (("QFull", 1), ("QEmpty", 1), ("OFull", 1), ("OEmpty", 4), ("StFull", 4), ("StEmpty", 4),
-                        ("SFull", 1), ("PFull", 4)):
+                        ("PFull", 4)):
             B[(name, t)] = Bar(c)
+        for i in range(2):
+            B[("SFull", t, i)] = Bar(1)
     for s in range(n_slots):
         B[("KVFull", s)] = Bar(2 if full_pairs else 1)
         B[("KVEmpty", s)] = Bar(1)
@@ -407,6 +428,7 @@ def simulate_default(units, kp, bf16, rng, d128=False, softmax_release=False, co
 
     def loader():
         ph_qe, kvc, nq = 0, 0, [0, 0]
+        g, cnt, hist = 0, [0, 0], [None, None]
         for (j0, n0, n1) in units:
             nkv = (n0, n1)
             for t in range(2):
@@ -416,17 +438,28 @@ def simulate_default(units, kp, bf16, rng, d128=False, softmax_release=False, co
                 ph_qe ^= 1 << t
                 nq[t] += 1
                 B[("QFull", t)].arrive()
-            for _ in range(j0, max(n0, n1)):
-                for _kind in range(2):
+            for j in range(j0, max(n0, n1)):
+                last = 1 if j < n1 else 0
+                info = (last, cnt[last])
+                for kind in range(2):
                     idx, s = kvc, kvc % n_slots
                     if idx >= n_slots:
-                        pr = (idx - n_slots + 1) // 2
-                        yield W(("KVEmpty", pr % n_pairs), (pr // n_pairs) & 1, pr // n_pairs)
+                        if loader_on_scores:
+                            sl, n = hist[(g + kind) & 1]
+                            yield W(("SFull", sl, n % n_sbars), (n // n_sbars) & 1, n // n_sbars)
+                        else:
+                            pr = (idx - n_slots + 1) // 2
+                            yield W(("KVEmpty", pr % n_pairs), (pr // n_pairs) & 1, pr // n_pairs)
                         old = slot_entry[s]
                         check(reads_left[old] == 0, f"ring entry {old} overwritten with {reads_left[old]} reads left")
+                    if kind == 0:
+                        hist[g & 1] = info
                     kvc += 1
                     slot_entry[s] = idx
                     B[("KVFull", (idx // 2) % n_pairs if full_pairs else s)].arrive()
+                for t in range(2):
+                    cnt[t] += j < nkv[t]
+                g += 1
 
     def converter():
         kvc = 0
@@ -467,11 +500,14 @@ def simulate_default(units, kp, bf16, rng, d128=False, softmax_release=False, co
             check(slot_entry[idx % n_slots] == idx, f"ring entry {idx} read while not in its slot")
             reads_left[idx] -= 1
 
+        sq = [0, 0]
+
         def qk(ui, t, j, idx):
             read_entry(idx)
             check(S[t] is None or S[t][2] == "done", f"QK of slot {t} step {j} overwrites {S[t]}")
             S[t] = (ui, j, "S")
-            B[("SFull", t)].arrive()
+            B[("SFull", t, sq[t])].arrive()
+            sq[t] = (sq[t] + 1) % n_sbars
 
         for ui, (j0, n0, n1) in enumerate(units):
             nkv, nmax = (n0, n1), max(n0, n1)
@@ -492,7 +528,7 @@ def simulate_default(units, kp, bf16, rng, d128=False, softmax_release=False, co
                 qk(ui, t, j0, kvb)
                 if nkv[t] == j0 + 1 and (not kp or t == qe_slot):
                     B[("QEmpty", 0 if kp else t)].arrive()
-            if not softmax_release:
+            if not softmax_release and not loader_on_scores:
                 release(kvb)
             for j in range(j0, nmax):
                 iv, ik = kvb + 2 * (j - j0) + 1, kvb + 2 * (j - j0) + 2
@@ -524,12 +560,13 @@ def simulate_default(units, kp, bf16, rng, d128=False, softmax_release=False, co
                         qk(ui, t, j + 1, ik)
                         if j + 1 == nkv[t] - 1 and (not kp or t == qe_slot):
                             B[("QEmpty", 0 if kp else t)].arrive()
-                if not softmax_release and j + 1 < nmax:
+                if not softmax_release and not loader_on_scores and j + 1 < nmax:
                     release(ik)
             kvc = kvb + 2 * (nmax - j0)
 
     def softmax(t, w):
-        ph_s = ph_te = ns = nte = 0
+        ph_te = nte = sb = 0
+        ns = [0, 0]
         kv_next = 0
         for ui, (j0, n0, n1) in enumerate(units):
             nkv = (n0, n1)[t]
@@ -538,9 +575,9 @@ def simulate_default(units, kp, bf16, rng, d128=False, softmax_release=False, co
             if nkv == 0:
                 continue
             for j in range(j0, nkv):
-                yield W(("SFull", t), ph_s, ns)
-                ph_s ^= 1
-                ns += 1
+                yield W(("SFull", t, sb), ns[sb] & 1, ns[sb])
+                ns[sb] += 1
+                sb = (sb + 1) % n_sbars
                 check(S[t] is not None and S[t][:2] == (ui, j), f"softmax {t} step {j} reads {S[t]}")
                 # O is stable: the commit that announced these scores covers the slot's previous P*V
                 check(pv_issued[(ui, t)] == j - j0, "scores announced with a P*V of the slot outstanding")

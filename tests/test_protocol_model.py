@@ -75,8 +75,8 @@ def _run_default(n_cases, kp, bf16, seed0=0, **kw):
     (False, True, dict(softmax_release=True)),
     (True, False, dict()),                                 # key-parity units (issuer commits)
     (True, True, dict()),
-    (False, True, dict(d128=True, covers_k=True)),         # D=128 bf16 (the converters cover K)
-    (False, False, dict(d128=True)),                       # D=128 fp16
+    (False, True, dict(d128=True, covers_k=True, loader_on_scores=True)),   # D=128 bf16: converters cover K,
+    (False, False, dict(d128=True, loader_on_scores=True)),                 # the loader waits on scores
 ])
 def test_default_protocol_holds(kp, bf16, kw):
     assert _run_default(80, kp, bf16, **kw) == 0
@@ -92,3 +92,24 @@ def test_softmax_release_would_break_key_parity_units():
 def test_model_catches_an_uncovered_k():
     # the issuer skipping its wait for K_{j+1} while the converters do not wait for it either
     assert _run_default(80, False, True, d128=True, covers_k=True, mistake="converter_skips_k") > 0
+
+
+def test_model_catches_one_score_barrier_per_slot():
+    # the loader waiting on scores can run one step behind them: with one
+    # score barrier per slot a parity wait aliases
+    assert _run_default(80, False, False, d128=True, loader_on_scores=True, mistake="one_score_barrier") > 0
+
+
+def test_loader_on_scores_would_alias_with_the_deeper_ring():
+    # at D=64 the two-tile ring has 8 entries: the loader runs up to three
+    # steps behind the scores, more than two barriers per slot can cover
+    from protocol_model import simulate_default
+    bad = 0
+    for c in range(80):
+        units = random_units(random.Random(c), False)
+        try:
+            ok, _ = simulate_default(units, False, False, random.Random(1000 * c), loader_on_scores=True)
+        except ProtocolError:
+            ok = False
+        bad += not ok
+    assert bad > 0
